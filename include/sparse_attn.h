@@ -1,0 +1,159 @@
+/*
+ * sparse_attn.h -- C ABI of the GB300 (sm_103a) Top-K block-sparse routed
+ * attention library (forward pass, one GPU, one process).
+ *
+ * The method (sources are web pages, cited by title and section):
+ *
+ *   Q, K, V are contiguous BF16 [B=1, T, H, 128] ("Sol-Attn and Spark for
+ *   MiniMax-H3", section "Install").  T is a target-video prefix of
+ *   `video_tokens` tokens followed by a context suffix (same page, "H3
+ *   pipeline integration").  Blocks are 64 tokens.  Let
+ *     nvk  = floor(video_tokens / 64)      full video blocks (routed keys)
+ *     nblk = ceil(T / 64)                  physical key blocks
+ *     sinks = blocks nvk .. nblk-1         context sink blocks (always exact)
+ *     K    = min(nvk, ceil(topk_ratio * nvk))
+ *   sparse_attn_plan mean-pools Q and K per block, scores every video query
+ *   block against every video key block, s = Qmean . Kmean / sqrt(128)
+ *   ("Spark inference integration": native mean Top-K routing, packed route
+ *   exported once), keeps the K best blocks by FP32 score (ties to the lower
+ *   index) among the non-local video blocks, and adds the self block, its
+ *   +-radius neighbours and every sink block outside the budget ("H3
+ *   pipeline integration", sol_exact_block_radius; "Add key bias to chunked
+ *   Sol-Attn producers", "Tests and source audit": sinks go straight into the
+ *   exact list).
+ *   sparse_attn_fwd runs exact softmax attention of each video query block
+ *   over the union of its list, and dense attention over every key for the
+ *   context rows and, with tail_mode = SA_TAIL_DENSE, for the rows of a video
+ *   block cut by the boundary ("H3 pipeline integration").  With
+ *   SA_TAIL_PAD that block is routed and attends sparsely; its centroid is
+ *   the mean of its real video rows.  An optional key bias in natural-log
+ *   units is added to the logits of sink keys only ("Add key bias to chunked
+ *   Sol-Attn producers", "Summary" and "Contract").
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers on the current CUDA device,
+ *     owned by the caller, 16-byte aligned and contiguous.  The library
+ *     allocates no device memory.
+ *   - All GPU work is enqueued on `stream`; plan and fwd never synchronise
+ *     the host.  Argument errors are returned before anything is enqueued.
+ *   - A workspace `ws` of the size reported by sparse_attn_query belongs to
+ *     one stream at a time; its first 256 bytes hold a device status word.
+ *   - No fallback: when the GPU path cannot run, the call fails.
+ */
+#ifndef SPARSE_ATTN_H_
+#define SPARSE_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SA_ABI_VERSION 1u
+
+typedef enum sa_status {
+  SA_OK = 0,
+  SA_EINVAL = 1,        /* bad argument, shape, pointer, size or key-bias value  */
+  SA_EUNSUPPORTED = 2,  /* outside what this build supports (B != 1, D != 128,
+                           a device that is not sm_103, sizes past the limits) */
+  SA_ENOSINKBIAS = 3,   /* nonzero key bias on a routed video key (u < 64 nvk)  */
+  SA_ECUDA = 4,         /* a CUDA runtime call or a kernel launch failed        */
+  SA_ETIMEOUT = 5       /* a bounded on-device wait gave up; outputs invalid    */
+} sa_status;
+
+typedef enum sa_tail_mode { SA_TAIL_DENSE = 0, SA_TAIL_PAD = 1 } sa_tail_mode;
+
+/* Problem description, passed by pointer to every call. */
+typedef struct sa_params {
+  uint32_t abi_version; /* must be SA_ABI_VERSION                               */
+  int32_t B;            /* batch, must be 1 (packed batch size one)             */
+  int32_t T;            /* packed tokens, >= 1                                  */
+  int32_t H;            /* heads, >= 1                                          */
+  int32_t D;            /* head dimension, must be 128                          */
+  int32_t video_tokens; /* target-video prefix length Nv, 64 <= Nv <= T         */
+  int32_t radius;       /* forced local radius R >= 0                           */
+  int32_t tail_mode;    /* sa_tail_mode                                         */
+  double topk_ratio;    /* Top-K ratio in (0, 1]; K = min(nvk, ceil(r * nvk)),
+                           the product rounded as a decimal: a relative slack
+                           of 1e-9 absorbs the binary representation of r     */
+} sa_params;
+
+/* Derived sizes and workspace requirements. */
+typedef struct sa_sizes {
+  int32_t nvk;             /* full video blocks                               */
+  int32_t tail;            /* video_tokens - 64 nvk                           */
+  int32_t nblk;            /* ceil(T / 64)                                    */
+  int32_t nq;              /* sparse query blocks: nvk, +1 for a pad tail     */
+  int32_t topk;            /* K                                               */
+  int32_t nsink;           /* nblk - nvk                                      */
+  int32_t maxl;            /* list width: min(nvk, 2R + 1 + K) + nsink        */
+  int32_t dense_row_start; /* first densely evaluated query row               */
+  uint64_t plan_ws_bytes;  /* workspace bytes for sparse_attn_plan            */
+  uint64_t fwd_ws_bytes;   /* workspace bytes for sparse_attn_fwd             */
+} sa_sizes;
+
+/*
+ * Validates `p` and fills `out`.  Host only: touches no device.
+ * Errors: SA_EINVAL (null pointer, abi_version mismatch, T < 1, H < 1,
+ * video_tokens outside [64, T], topk_ratio outside (0, 1], radius < 0,
+ * unknown tail_mode, pad mode with T < 64 (nvk + 1) when the video tail is
+ * nonempty); SA_EUNSUPPORTED (B != 1, D != 128, nvk > 8192, maxl > 1024,
+ * T * H * 128 beyond 2^31 elements).
+ */
+sa_status sparse_attn_query(const sa_params* p, sa_sizes* out);
+
+/*
+ * Routing: pool + route scores + Top-K + block lists.
+ *   q, k          BF16 [1, T, H, 128]
+ *   idx           int32 [1, H, nq, maxl]: row (h, i) holds the sorted block
+ *                 list of query block i in head h, padded with -1
+ *   cnt           int32 [1, H, nq]: list lengths
+ *   route_scores  optional (may be NULL) float32 [H, nq, nvk]: the scores
+ *                 the selection compared (Qmean . Kmean / sqrt(128))
+ *   ws, ws_bytes  workspace of at least plan_ws_bytes.  Layout after the
+ *                 256-byte status area: Qmean float32 [H, nq, 128], then
+ *                 Kmean float32 [H, nvk, 128], each 256-byte aligned.
+ * Errors before launch: as sparse_attn_query, plus SA_EINVAL for a null or
+ * misaligned required pointer or a short workspace.  SA_ECUDA if a launch
+ * fails.
+ */
+sa_status sparse_attn_plan(const sa_params* p, const void* q, const void* k, int32_t* idx,
+                           int32_t* cnt, float* route_scores, void* ws, size_t ws_bytes,
+                           cudaStream_t stream);
+
+/*
+ * Attention: sparse video blocks over their lists, dense rows over all keys.
+ *   q, k, v   BF16 [1, T, H, 128]
+ *   key_bias  optional (may be NULL) float32 [B * T] in natural-log units.
+ *             Converted once to log2 units.  Must be 0 on every key
+ *             u < 64 nvk (else SA_ENOSINKBIAS); NaN or +inf anywhere gives
+ *             SA_EINVAL; -inf removes the key.  Both are device-detected:
+ *             read them with sparse_attn_last_device_status.
+ *   idx, cnt  block lists from sparse_attn_plan (same params)
+ *   o         BF16 [1, T, H, 128]; every row is written when the device
+ *             status is SA_OK
+ *   ws        workspace of at least fwd_ws_bytes (may alias none of the
+ *             tensors above)
+ * Errors before launch: as sparse_attn_plan.  Device-detected conditions
+ * leave `o` unspecified and are reported by sparse_attn_last_device_status.
+ */
+sa_status sparse_attn_fwd(const sa_params* p, const void* q, const void* k, const void* v,
+                          const float* key_bias, const int32_t* idx, const int32_t* cnt, void* o,
+                          void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Reads the device status word of `ws` (written by the last plan or fwd
+ * enqueued with it).  Synchronises `stream`.  SA_ECUDA if the copy fails.
+ */
+sa_status sparse_attn_last_device_status(const void* ws, cudaStream_t stream, sa_status* out);
+
+/* Static, human-readable name of a status code. */
+const char* sparse_attn_status_string(sa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSE_ATTN_H_ */
