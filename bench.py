@@ -1,0 +1,445 @@
+"""Benchmark: Top-K block-sparse routed attention, plan + fwd, on one GB300.
+
+A step is one pass of the whole path (pool, route + Top-K + lists, attention
+over the lists, dense rows) over the H3-shaped workload: 9505 packed tokens
+(9240 video + 265 context), 56 heads, head dim 128, BF16, Top-K ratio 0.1,
+radius 1, dense tail.  Inputs are synthetic (block-clustered random walks,
+seeded) and resident in HBM; Q + K + V + O = 545 MB is larger than the 126 MB
+L2, so no flush is needed between steps.
+
+The metric is kept-block attention TFLOP/s: 4 * 128 FLOP per (real query
+row, kept key) pair, summed over heads, divided by the step time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Rank 0 prints one JSON line.  With N > 1 (torchrun), every rank runs its own
+independent copy of the workload (weak scaling: heads and problems are
+independent, no collective in the data path); the timing is the max over
+ranks.  ``--impl reference`` times the CPU fp64 oracle on the host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import multiprocessing as mp
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "kept-block attention TFLOP/s and ms/call at 9505 tok × 56 heads; % BF16 peak"
+WORKLOAD = "h3"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attention_kernel_h3.md")
+ATTN_SOURCE = os.path.join(ROOT, "block_sparse_routed_gb300", "csrc", "attn_kernel.cu")
+
+
+# ----------------------------------------------------------------- helpers
+def kept_pairs_from_lists(idx, cnt, T, nvk, nq, Nv, dense_row_start):
+    """Kept (query row, key) pairs given the block lists (host count)."""
+    cnt = cnt.reshape(-1, nq)
+    H = cnt.shape[0]
+    idx = idx.reshape(H, nq, -1)
+    blk_len = np.minimum(64, T - 64 * np.arange((T + 63) // 64))
+    total = 0
+    for i in range(nq):
+        rows = 64 if i < nvk else Nv - 64 * nvk
+        for h in range(H):
+            lst = idx[h, i, : cnt[h, i]]
+            total += rows * int(blk_len[lst].sum())
+    total += H * (T - dense_row_start) * T
+    return total
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def profile_traffic():
+    """Per-launch DRAM bytes of the attention kernel from the committed ncu
+    summary, or None when the kernel source changed since it was taken."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    txt = open(PROFILE_SUMMARY).read()
+    m_t = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", txt)
+    m_h = re.search(r"attn_kernel_sha256:\s*([0-9a-f]+)", txt)
+    if not (m_t and m_h):
+        return None
+    cur = hashlib.sha256(open(ATTN_SOURCE, "rb").read()).hexdigest()
+    if not cur.startswith(m_h.group(1)):
+        return None
+    return int(m_t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- CPU oracle legs
+def _oracle_worker(args):
+    """Times the oracle on one head slice (runs in a spawned process)."""
+    q, k, v, bias, prm = args
+    import oracle as O
+
+    sz = O.derive_sizes(prm["T"], q.shape[1], prm["video_tokens"], prm["topk_ratio"],
+                        prm["radius"], prm["tail_mode"])
+    t0 = time.perf_counter()
+    ref = O.plan(q, k, sz)
+    O.forward(q, k, v, bias, ref["idx"], ref["cnt"], sz)
+    dt = time.perf_counter() - t0
+    return O.kept_flops(ref["idx"], ref["cnt"], sz), dt
+
+
+def _oracle_pool(ncores):
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"  # one BLAS thread per worker process
+    return mp.get_context("spawn").Pool(ncores)
+
+
+def oracle_timing(pool, arrays, prm, heads_per_task, ncores, heads):
+    """Wall time of the oracle over `heads` (a list of head indices), spread
+    over the pool; returns (kept_flops, seconds)."""
+    tasks = []
+    for i in range(0, len(heads), heads_per_task):
+        hs = heads[i:i + heads_per_task]
+        tasks.append((np.ascontiguousarray(arrays["q"][:, hs]), np.ascontiguousarray(arrays["k"][:, hs]),
+                      np.ascontiguousarray(arrays["v"][:, hs]), arrays["bias"], prm))
+    t0 = time.perf_counter()
+    res = pool.map(_oracle_worker, tasks, chunksize=1)
+    wall = time.perf_counter() - t0
+    return sum(r[0] for r in res), wall
+
+
+# ----------------------------------------------------------------- main legs
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, timed on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    from workloads import make_workload
+
+    arrays, prm = make_workload(WORKLOAD)
+    ncores = host_cores()
+    pool = _oracle_pool(ncores)
+    H = prm["H"]
+    sample_heads = list(range(min(H, ncores)))  # one head per core per step
+    try:
+        for _ in range(args.warmup):
+            oracle_timing(pool, arrays, prm, 1, ncores, sample_heads[:1])
+        flops, secs = 0, 0.0
+        for _ in range(args.steps):
+            f, s = oracle_timing(pool, arrays, prm, 1, ncores, sample_heads)
+            flops += f
+            secs += s
+    finally:
+        pool.close()
+        pool.join()
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": args.gpus,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": workload_config(prm),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": ncores, "kind": "oracle",
+                         "sample": f"{len(sample_heads)} of {H} heads per step, all rows"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(prm):
+    return {
+        "workload": "H3-shaped packed video sequence (9240 video + 265 context tokens)",
+        "T": prm["T"],
+        "H": prm["H"],
+        "head_dim": 128,
+        "video_tokens": prm["video_tokens"],
+        "topk_ratio": prm["topk_ratio"],
+        "radius": prm["radius"],
+        "tail_mode": prm["tail_mode"],
+        "key_bias": None,
+        "l2": "inputs larger than L2 (Q+K+V+O 545 MB > 126 MB), no flush",
+    }
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import block_sparse_routed_gb300 as bsr
+    from workloads import make_workload
+
+    # CPU baseline pool first: spawned before the first GPU call.
+    pool = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        pool = _oracle_pool(host_cores())
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    bsr.load_library()
+    arrays, prm = make_workload(WORKLOAD)
+    T, H, Nv = prm["T"], prm["H"], prm["video_tokens"]
+    P = bsr.Params(T=T, H=H, video_tokens=Nv, topk_ratio=prm["topk_ratio"], radius=prm["radius"],
+                   tail_mode=prm["tail_mode"])
+    sz = bsr.sparse_attn_query(P)
+
+    def pinned(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).reshape(1, T, H, 128).pin_memory()
+
+    hq, hk, hv = pinned(arrays["q"]), pinned(arrays["k"]), pinned(arrays["v"])
+    q, k, v = hq.to(dev), hk.to(dev), hv.to(dev)
+    bias = None
+    if arrays["bias"] is not None:
+        hbias = torch.from_numpy(arrays["bias"]).pin_memory()
+        bias = hbias.to(dev)
+    idx = torch.empty((1, H, sz.nq, sz.maxl), dtype=torch.int32, device=dev)
+    cnt = torch.empty((1, H, sz.nq), dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    ws_plan = torch.empty(sz.plan_ws_bytes, dtype=torch.uint8, device=dev)
+    ws_fwd = torch.empty(sz.fwd_ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        bsr.sparse_attn_plan(P, q, k, idx=idx, cnt=cnt, ws=ws_plan, stream=stream)
+        bsr.sparse_attn_fwd(P, q, k, v, idx, cnt, key_bias=bias, o=o, ws=ws_fwd, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    st = bsr.sparse_attn_last_device_status(ws_fwd, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+    kept = kept_pairs_from_lists(idx.cpu().numpy(), cnt.cpu().numpy(), T, sz.nvk, sz.nq, Nv,
+                                 sz.dense_row_start) * 4 * 128
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # ---- device-resident timing: per-step events split plan / fwd
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        ev[s][0].record(stream)
+        bsr.sparse_attn_plan(P, q, k, idx=idx, cnt=cnt, ws=ws_plan, stream=stream)
+        ev[s][1].record(stream)
+        bsr.sparse_attn_fwd(P, q, k, v, idx, cnt, key_bias=bias, o=o, ws=ws_fwd, stream=stream)
+        ev[s][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    plan_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
+    fwd_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(args.steps)]
+    if bsr.sparse_attn_last_device_status(ws_fwd, stream) != 0:
+        raise RuntimeError("device status error in the timed region")
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * kept / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end through the public API, host buffers
+    ho = torch.empty((1, T, H, 128), dtype=torch.bfloat16).pin_memory()
+    h2d = 3 * T * H * 128 * 2 + (T * 4 if bias is not None else 0)
+    d2h = T * H * 128 * 2
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        if bias is not None:
+            bias.copy_(hbias, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * kept / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        return
+
+    peaks, peak_kind = measured_peaks()
+    fwd_avg = sum(fwd_ms) / len(fwd_ms)
+    achieved = kept / (fwd_avg * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": profile_traffic(),
+                "kernel": "attention_kernel (fwd call: status memset + attention)",
+                "peak_kind": f"{peak_kind} bf16 burst"}
+
+    cpu = None
+    if pool is not None:
+        try:
+            heads = list(range(H))
+            flops_c, secs_c = oracle_timing(pool, arrays, prm, 1, host_cores(), heads)
+            cpu = {"value": flops_c / secs_c / 1e12, "unit": "TFLOP/s", "cores": host_cores(),
+                   "kind": "oracle", "seconds": secs_c,
+                   "sample": f"whole workload ({H} heads, all rows), one head per task, "
+                             f"one BLAS thread per worker"}
+        finally:
+            pool.close()
+            pool.join()
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": workload_config(prm),
+        "plan_ms": sum(plan_ms) / len(plan_ms),
+        "fwd_ms": fwd_avg,
+        "kept_tflop_per_step": kept / 1e12,
+        "frac_of_bf16_peak": value / world / peak,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * (3 + (1 if bias is not None else 0)),
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,193 @@
+"""Top-K block-sparse routed attention for one GB300 (sm_103a).
+
+Two calls, backed by hand-written CUDA kernels in a C-ABI library:
+
+* ``sparse_attn_plan``: mean-pools Q and K over 64-token blocks, scores video
+  query blocks against video key blocks, selects the Top-K key blocks per
+  query block and writes sorted per-block lists (forced local blocks and
+  context sink blocks included).
+* ``sparse_attn_fwd``: exact softmax attention of each video query block over
+  its list, dense attention for context rows (and a dense video tail), with
+  an optional natural-log key bias on sink keys.
+
+This module marshals torch tensors to the C entry points of the same names.
+PyTorch provides device memory and streams only; every step runs in the
+library's kernels.  There is no CPU fallback.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+from . import _native
+from ._native import (  # noqa: F401
+    SA_EINVAL,
+    SA_ENOSINKBIAS,
+    SA_ETIMEOUT,
+    SA_EUNSUPPORTED,
+    SA_OK,
+    SaParams,
+    SaSizes,
+    SparseAttnError,
+    load_library,
+    sparse_attn_status_string,
+)
+
+__all__ = [
+    "Params",
+    "SparseAttnError",
+    "load_library",
+    "sparse_attn",
+    "sparse_attn_fwd",
+    "sparse_attn_last_device_status",
+    "sparse_attn_plan",
+    "sparse_attn_query",
+    "sparse_attn_status_string",
+]
+
+
+@dataclass(frozen=True)
+class Params:
+    """Problem description (mirrors ``sa_params``)."""
+
+    T: int
+    H: int
+    video_tokens: int
+    topk_ratio: float
+    radius: int = 1
+    tail_mode: str = "dense"  # "dense" or "pad"
+    B: int = 1
+    D: int = 128
+
+    def to_c(self) -> SaParams:
+        modes = {"dense": _native.SA_TAIL_DENSE, "pad": _native.SA_TAIL_PAD}
+        if self.tail_mode not in modes:
+            raise ValueError("tail_mode must be 'dense' or 'pad'")
+        return SaParams(
+            _native.SA_ABI_VERSION,
+            self.B,
+            self.T,
+            self.H,
+            self.D,
+            self.video_tokens,
+            self.radius,
+            modes[self.tail_mode],
+            float(self.topk_ratio),
+        )
+
+
+def sparse_attn_query(params: Params) -> SaSizes:
+    """Derived sizes and workspace bytes (host only)."""
+    return _native.sparse_attn_query(params.to_c())
+
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _check_qkv(t, name, params):
+    torch = _torch()
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    shape = tuple(t.shape)
+    if shape not in ((params.B, params.T, params.H, params.D), (params.T, params.H, params.D)):
+        raise ValueError(f"{name} must have shape [1, T, H, 128], got {shape}")
+
+
+def _stream_handle(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _workspace(nbytes, device):
+    torch = _torch()
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def sparse_attn_plan(params: Params, q, k, idx=None, cnt=None, route_scores=None, ws=None,
+                     stream=None):
+    """Block lists for (q, k).  Returns (idx int32 [1,H,nq,maxl], cnt int32 [1,H,nq]).
+
+    Missing outputs and workspace are allocated with torch on q's device.
+    Pass ``route_scores`` (float32 [H, nq, nvk]) to receive the scores.
+    """
+    torch = _torch()
+    _check_qkv(q, "q", params)
+    _check_qkv(k, "k", params)
+    cp = params.to_c()
+    sz = _native.sparse_attn_query(cp)
+    dev = q.device
+    if idx is None:
+        idx = torch.empty((1, params.H, sz.nq, sz.maxl), dtype=torch.int32, device=dev)
+    if cnt is None:
+        cnt = torch.empty((1, params.H, sz.nq), dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = _workspace(sz.plan_ws_bytes, dev)
+    for t, n, want in ((idx, "idx", params.H * sz.nq * sz.maxl), (cnt, "cnt", params.H * sz.nq)):
+        if t.dtype != torch.int32 or not t.is_contiguous() or t.numel() != want:
+            raise ValueError(f"{n}: int32 contiguous tensor with {want} elements required")
+    rs = 0
+    if route_scores is not None:
+        if route_scores.dtype != torch.float32 or route_scores.numel() != params.H * sz.nq * sz.nvk:
+            raise ValueError("route_scores: float32 [H, nq, nvk] required")
+        rs = route_scores.data_ptr()
+    st = _native.sparse_attn_plan(cp, q.data_ptr(), k.data_ptr(), idx.data_ptr(), cnt.data_ptr(),
+                                  rs, ws.data_ptr(), ws.numel(), _stream_handle(stream))
+    if st != SA_OK:
+        raise SparseAttnError(st, "sparse_attn_plan")
+    return idx, cnt
+
+
+def sparse_attn_fwd(params: Params, q, k, v, idx, cnt, key_bias=None, o=None, ws=None,
+                    stream=None):
+    """Attention output o (bf16, same shape as q).  The device status of the
+    call is read with ``sparse_attn_last_device_status(ws)``."""
+    torch = _torch()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_qkv(t, n, params)
+    cp = params.to_c()
+    sz = _native.sparse_attn_query(cp)
+    if key_bias is not None:
+        # the bias carrier: packed contiguous float32 with exactly B*T elements
+        if (key_bias.dtype != torch.float32 or not key_bias.is_contiguous()
+                or key_bias.numel() != params.B * params.T or not key_bias.is_cuda):
+            raise ValueError("key_bias must be a contiguous CUDA float32 tensor with B*T elements")
+    if o is None:
+        o = torch.empty_like(q)
+    _check_qkv(o, "o", params)
+    if ws is None:
+        ws = _workspace(sz.fwd_ws_bytes, q.device)
+    st = _native.sparse_attn_fwd(cp, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                 key_bias.data_ptr() if key_bias is not None else 0,
+                                 idx.data_ptr(), cnt.data_ptr(), o.data_ptr(), ws.data_ptr(),
+                                 ws.numel(), _stream_handle(stream))
+    if st != SA_OK:
+        raise SparseAttnError(st, "sparse_attn_fwd")
+    return o
+
+
+def sparse_attn_last_device_status(ws, stream=None) -> int:
+    """Device status word of a workspace (synchronises the stream)."""
+    return _native.sparse_attn_last_device_status(ws.data_ptr(), _stream_handle(stream))
+
+
+def sparse_attn(params: Params, q, k, v, key_bias=None, check_status=True, stream=None):
+    """plan + fwd in one call; raises on a device-detected error when
+    ``check_status`` (which synchronises the stream)."""
+    sz = _native.sparse_attn_query(params.to_c())
+    ws = _workspace(max(sz.plan_ws_bytes, sz.fwd_ws_bytes), q.device)
+    idx, cnt = sparse_attn_plan(params, q, k, ws=ws, stream=stream)
+    o = sparse_attn_fwd(params, q, k, v, idx, cnt, key_bias=key_bias, ws=ws, stream=stream)
+    if check_status:
+        st = sparse_attn_last_device_status(ws, stream)
+        if st != SA_OK:
+            raise SparseAttnError(st, "sparse_attn (device)")
+    return o

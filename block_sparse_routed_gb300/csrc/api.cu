@@ -1,0 +1,233 @@
+// Host side of the C ABI declared in include/sparse_attn.h: argument
+// validation, derived sizes, workspace layout, TMA descriptors and launch
+// sequencing.  Every check happens before anything is enqueued; there is no
+// fallback path.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+#include "sparse_attn.h"
+
+#define SA_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+using namespace sa;
+
+constexpr uint64_t align256(uint64_t x) { return (x + 255u) & ~uint64_t(255); }
+
+sa_status derive(const sa_params* p, Geometry* g, sa_sizes* out) {
+  if (p == nullptr) return SA_EINVAL;
+  if (p->abi_version != SA_ABI_VERSION) return SA_EINVAL;
+  if (p->B != 1 || p->D != kHeadDim) return SA_EUNSUPPORTED;
+  if (p->T < 1 || p->H < 1) return SA_EINVAL;
+  if (p->video_tokens < kBlock || p->video_tokens > p->T) return SA_EINVAL;
+  if (!(p->topk_ratio > 0.0 && p->topk_ratio <= 1.0)) return SA_EINVAL;
+  if (p->radius < 0) return SA_EINVAL;
+  if (p->tail_mode != SA_TAIL_DENSE && p->tail_mode != SA_TAIL_PAD) return SA_EINVAL;
+  const int64_t T = p->T, H = p->H, Nv = p->video_tokens;
+  const int64_t nvk = Nv / kBlock;
+  const int64_t tail = Nv - kBlock * nvk;
+  const int64_t nblk = (T + kBlock - 1) / kBlock;
+  const bool pad = p->tail_mode == SA_TAIL_PAD && tail > 0;
+  if (pad && T < kBlock * (nvk + 1)) return SA_EINVAL;
+  if (T * H * kHeadDim >= (int64_t(1) << 31)) return SA_EUNSUPPORTED;
+  if (nvk > kMaxVideoBlocks) return SA_EUNSUPPORTED;
+  const int64_t nq = nvk + (pad ? 1 : 0);
+  // K = ceil(r * nvk) taken on the decimal value of r: a relative slack of
+  // 1e-9 absorbs the binary representation error of r (0.1 * 30 -> 3).
+  const double prod = p->topk_ratio * static_cast<double>(nvk);
+  int64_t K = static_cast<int64_t>(std::ceil(prod - 1e-9 * prod));
+  if (K < 1) K = 1;
+  if (K > nvk) K = nvk;
+  const int64_t R = p->radius;
+  const int64_t nsink = nblk - nvk;
+  const int64_t local = (2 * R + 1 + K < nvk) ? 2 * R + 1 + K : nvk;
+  const int64_t maxl = local + nsink;
+  if (maxl > kMaxList) return SA_EUNSUPPORTED;
+  const int64_t r0 = (p->tail_mode == SA_TAIL_DENSE) ? kBlock * nvk : Nv;
+  if (g) {
+    g->T = static_cast<int>(T);
+    g->H = static_cast<int>(H);
+    g->Nv = static_cast<int>(Nv);
+    g->nvk = static_cast<int>(nvk);
+    g->tail = static_cast<int>(tail);
+    g->nblk = static_cast<int>(nblk);
+    g->nq = static_cast<int>(nq);
+    g->K = static_cast<int>(K);
+    g->R = static_cast<int>(R > nvk ? nvk : R);
+    g->pad = pad ? 1 : 0;
+    g->nsink = static_cast<int>(nsink);
+    g->maxl = static_cast<int>(maxl);
+    g->r0 = static_cast<int>(r0);
+  }
+  if (out) {
+    out->nvk = static_cast<int32_t>(nvk);
+    out->tail = static_cast<int32_t>(tail);
+    out->nblk = static_cast<int32_t>(nblk);
+    out->nq = static_cast<int32_t>(nq);
+    out->topk = static_cast<int32_t>(K);
+    out->nsink = static_cast<int32_t>(nsink);
+    out->maxl = static_cast<int32_t>(maxl);
+    out->dense_row_start = static_cast<int32_t>(r0);
+    out->plan_ws_bytes = kStatusBytes + align256(uint64_t(H) * nq * kHeadDim * 4) +
+                         align256(uint64_t(H) * nvk * kHeadDim * 4);
+    out->fwd_ws_bytes = kStatusBytes + align256(uint64_t(T) * 4);
+  }
+  return SA_OK;
+}
+
+bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+// Per-device check that the current device is an sm_103 part (this library
+// carries sm_103a code only).  Cached: one attribute query per device.
+sa_status check_device() {
+  static std::mutex mu;
+  static signed char state[128] = {0};  // 0 unknown, 1 ok, -1 unsupported
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SA_ECUDA;
+  if (dev < 0 || dev >= 128) return SA_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(mu);
+  if (state[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return SA_ECUDA;
+    state[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  return state[dev] == 1 ? SA_OK : SA_EUNSUPPORTED;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2-D view [T rows, H*128 columns] of a BF16 [T, H, 128] tensor, box of 64
+// columns (128 bytes, one swizzle row) x box_rows rows, 128-byte swizzle,
+// zero fill past the last row.
+bool make_map(CUtensorMap* m, const void* ptr, const Geometry& g, uint32_t box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(g.H) * kHeadDim, static_cast<cuuint64_t>(g.T)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(g.H) * kHeadDim * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+SA_API sa_status sparse_attn_query(const sa_params* p, sa_sizes* out) {
+  if (out == nullptr) return SA_EINVAL;
+  return derive(p, nullptr, out);
+}
+
+SA_API sa_status sparse_attn_plan(const sa_params* p, const void* q, const void* k, int32_t* idx,
+                                  int32_t* cnt, float* route_scores, void* ws, size_t ws_bytes,
+                                  cudaStream_t stream) {
+  Geometry g;
+  sa_sizes sz;
+  sa_status st = derive(p, &g, &sz);
+  if (st != SA_OK) return st;
+  if (!q || !k || !idx || !cnt || !ws) return SA_EINVAL;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(idx, 4) || !aligned(cnt, 4) ||
+      !aligned(ws, 256) || (route_scores && !aligned(route_scores, 4)))
+    return SA_EINVAL;
+  if (ws_bytes < sz.plan_ws_bytes) return SA_EINVAL;
+  st = check_device();
+  if (st != SA_OK) return st;
+
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  PlanArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = static_cast<const uint16_t*>(k);
+  a.qc = reinterpret_cast<float*>(w + kStatusBytes);
+  a.kc = reinterpret_cast<float*>(w + kStatusBytes +
+                                  align256(uint64_t(g.H) * g.nq * kHeadDim * 4));
+  a.idx = idx;
+  a.cnt = cnt;
+  a.scores = route_scores;
+  a.g = g;
+  if (cudaMemsetAsync(ws, 0, kStatusBytes, stream) != cudaSuccess) return SA_ECUDA;
+  if (launch_pool(a, stream) != cudaSuccess) return SA_ECUDA;
+  if (launch_route_topk(a, stream) != cudaSuccess) return SA_ECUDA;
+  return SA_OK;
+}
+
+SA_API sa_status sparse_attn_fwd(const sa_params* p, const void* q, const void* k, const void* v,
+                                 const float* key_bias, const int32_t* idx, const int32_t* cnt,
+                                 void* o, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  Geometry g;
+  sa_sizes sz;
+  sa_status st = derive(p, &g, &sz);
+  if (st != SA_OK) return st;
+  if (!q || !k || !v || !idx || !cnt || !o || !ws) return SA_EINVAL;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(idx, 4) || !aligned(cnt, 4) || !aligned(ws, 256) ||
+      (key_bias && !aligned(key_bias, 4)))
+    return SA_EINVAL;
+  if (ws_bytes < sz.fwd_ws_bytes) return SA_EINVAL;
+  st = check_device();
+  if (st != SA_OK) return st;
+
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, q, g, 128) || !make_map(&tk, k, g, 64) || !make_map(&tv, v, g, 64))
+    return SA_ECUDA;
+
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* status = reinterpret_cast<int32_t*>(w);
+  float* b2 = key_bias ? reinterpret_cast<float*>(w + kStatusBytes) : nullptr;
+  if (cudaMemsetAsync(ws, 0, kStatusBytes, stream) != cudaSuccess) return SA_ECUDA;
+  if (key_bias && launch_bias_prep(key_bias, b2, status, g, stream) != cudaSuccess) return SA_ECUDA;
+
+  AttnArgs a;
+  a.idx = idx;
+  a.cnt = cnt;
+  a.b2 = b2;
+  a.o = static_cast<uint16_t*>(o);
+  a.status = status;
+  a.g = g;
+  a.n_dense = (g.T - g.r0 + 127) / 128;
+  a.n_pairs = (g.nq + 1) / 2;
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(128.0));
+  if (launch_attention(tq, tk, tv, a, stream) != cudaSuccess) return SA_ECUDA;
+  return SA_OK;
+}
+
+SA_API sa_status sparse_attn_last_device_status(const void* ws, cudaStream_t stream,
+                                                sa_status* out) {
+  if (!ws || !out) return SA_EINVAL;
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return SA_ECUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return SA_ECUDA;
+  *out = static_cast<sa_status>(v);
+  return SA_OK;
+}
+
+SA_API const char* sparse_attn_status_string(sa_status s) {
+  switch (s) {
+    case SA_OK: return "SA_OK";
+    case SA_EINVAL: return "SA_EINVAL: invalid argument";
+    case SA_EUNSUPPORTED: return "SA_EUNSUPPORTED: unsupported shape or device";
+    case SA_ENOSINKBIAS: return "SA_ENOSINKBIAS: key bias on a routed video key";
+    case SA_ECUDA: return "SA_ECUDA: CUDA error";
+    case SA_ETIMEOUT: return "SA_ETIMEOUT: on-device wait timed out";
+  }
+  return "unknown sa_status";
+}

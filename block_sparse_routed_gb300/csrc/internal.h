@@ -1,0 +1,65 @@
+// Definitions shared by the host side of the C ABI and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace sa {
+
+constexpr int kBlock = 64;         // tokens per physical block
+constexpr int kHeadDim = 128;      // head dimension
+constexpr int kStatusBytes = 256;  // device status area at the start of a workspace
+constexpr int kMaxList = 1024;     // largest supported block-list width (maxl)
+constexpr int kMaxVideoBlocks = 8192;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded on-device waits: 1 s
+
+// Block bookkeeping derived from sa_params (see sparse_attn.h).
+struct Geometry {
+  int T, H, Nv;
+  int nvk;    // full video blocks
+  int tail;   // Nv - 64 nvk
+  int nblk;   // ceil(T / 64)
+  int nq;     // sparse query blocks
+  int K;      // Top-K budget
+  int R;      // forced local radius
+  int pad;    // 1 when the video tail block is routed (pad mode with tail > 0)
+  int nsink;  // nblk - nvk
+  int maxl;   // block-list width
+  int r0;     // first dense query row
+};
+
+struct PlanArgs {
+  const uint16_t* q;  // BF16 bits [T, H, 128]
+  const uint16_t* k;
+  float* qc;          // [H, nq, 128]
+  float* kc;          // [H, nvk, 128]
+  int32_t* idx;       // [H, nq, maxl]
+  int32_t* cnt;       // [H, nq]
+  float* scores;      // [H, nq, nvk] or null
+  Geometry g;
+};
+
+struct AttnArgs {
+  const int32_t* idx;
+  const int32_t* cnt;
+  const float* b2;     // key bias in log2 units [T], or null
+  uint16_t* o;         // BF16 bits [T, H, 128]
+  int32_t* status;     // device status word
+  Geometry g;
+  int n_dense;         // dense 128-row tiles per head
+  int n_pairs;         // sparse query-block pairs per head
+  float scale_log2;    // log2(e) / sqrt(128)
+};
+
+// Launchers (defined in the kernel translation units).
+cudaError_t launch_pool(const PlanArgs& a, cudaStream_t s);
+cudaError_t launch_route_topk(const PlanArgs& a, cudaStream_t s);
+cudaError_t launch_bias_prep(const float* bias, float* b2, int32_t* status, const Geometry& g,
+                             cudaStream_t s);
+cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const AttnArgs& a, cudaStream_t s);
+size_t route_topk_smem_bytes(const Geometry& g);
+size_t attention_smem_bytes();
+
+}  // namespace sa

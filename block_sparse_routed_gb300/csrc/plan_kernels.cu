@@ -1,0 +1,239 @@
+// Routing kernels: block mean pooling, and route scores + Top-K + block-list
+// compaction.
+//
+// Pooling follows "Sol-Attn and Spark for MiniMax-H3", section "Spark
+// inference integration" (native mean Top-K routing): the route centroid of
+// a 64-token block is the mean of its rows; in pad mode the tail block's
+// centroid is the mean of its real video rows (section "H3 pipeline
+// integration").  Route scores are Qmean . Kmean / sqrt(128) in FP32; the
+// Top-K boundary is found by an exact radix search over FP32 keys (the same
+// page names "exact FP32 radix boundary selection"), ties going to the lower
+// block index.  Forced local blocks (self +- radius) are not candidates and
+// are added outside the budget; sink blocks are always in the list ("Add key
+// bias to chunked Sol-Attn producers", "Tests and source audit").
+#include <cstdint>
+
+#include "internal.h"
+
+namespace sa {
+namespace {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// One CTA per (block, tensor): blockIdx.y = 0 pools Q over the nq query
+// blocks, 1 pools K over the nvk video key blocks.  Each thread owns 16-byte
+// column slices of a token row (8 dims of one head) and sums them down the
+// block's rows; consecutive threads read consecutive 16-byte slices, so every
+// row is read with full coalescing.  HBM-bound.
+__global__ void __launch_bounds__(256) pool_kernel(PlanArgs a) {
+  const Geometry& g = a.g;
+  const bool isq = blockIdx.y == 0;
+  const int nblocks = isq ? g.nq : g.nvk;
+  const int i = blockIdx.x;
+  if (i >= nblocks) return;
+  const int n = (i < g.nvk) ? kBlock : g.tail;  // the pad tail block owns `tail` rows
+  const uint4* src = reinterpret_cast<const uint4*>(isq ? a.q : a.k);
+  float* dst = isq ? a.qc : a.kc;
+  const int vpr = g.H * (kHeadDim / 8);  // 16-byte slices per token row
+  const float fn = static_cast<float>(n);
+  for (int c = threadIdx.x; c < vpr; c += blockDim.x) {
+    const uint4* p = src + static_cast<size_t>(i) * kBlock * vpr + c;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int r = 0; r < n; ++r) {
+      const uint4 v = __ldg(p + static_cast<size_t>(r) * vpr);
+      acc[0] += bf16_lo(v.x); acc[1] += bf16_hi(v.x);
+      acc[2] += bf16_lo(v.y); acc[3] += bf16_hi(v.y);
+      acc[4] += bf16_lo(v.z); acc[5] += bf16_hi(v.z);
+      acc[6] += bf16_lo(v.w); acc[7] += bf16_hi(v.w);
+    }
+    const int h = c / (kHeadDim / 8);
+    const int d0 = (c % (kHeadDim / 8)) * 8;
+    float4* o = reinterpret_cast<float4*>(dst + (static_cast<size_t>(h) * nblocks + i) * kHeadDim + d0);
+    o[0] = make_float4(acc[0] / fn, acc[1] / fn, acc[2] / fn, acc[3] / fn);
+    o[1] = make_float4(acc[4] / fn, acc[5] / fn, acc[6] / fn, acc[7] / fn);
+  }
+}
+
+// Order-preserving map of an FP32 score to an unsigned key; -0 and +0 map to
+// the same key.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (f == 0.0f) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+constexpr int kRouteThreads = 256;
+constexpr int kKeyChunk = 64;        // Kmean rows staged per step
+constexpr int kKcStride = kHeadDim + 1;  // padded row: conflict-free column reads
+
+// One CTA per (QB query blocks, head).  Phase 1: the QB x nvk score strip in
+// shared memory, FP32 FMA over d = 0..127 in order.  Phase 2: one warp per
+// query block runs the radix search for the K'-th largest key and emits the
+// sorted union of forced local blocks, selected blocks and sinks.
+template <int QB>
+__global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
+  const Geometry& g = a.g;
+  extern __shared__ __align__(16) float rsm[];
+  float* qcT = rsm;                              // [128][QB]
+  float* kcs = qcT + kHeadDim * QB;              // [64][129]
+  float* sc = kcs + kKeyChunk * kKcStride;       // [QB][nvk]
+  const int h = blockIdx.y;
+  const int i0 = blockIdx.x * QB;
+  const int tid = threadIdx.x;
+
+  for (int e = tid; e < QB * kHeadDim; e += kRouteThreads) {
+    const int qi = e / kHeadDim, d = e % kHeadDim;
+    const int i = i0 + qi;
+    qcT[d * QB + qi] = (i < g.nq) ? a.qc[(static_cast<size_t>(h) * g.nq + i) * kHeadDim + d] : 0.f;
+  }
+
+  constexpr int QPT = QB / 4;  // query blocks per thread
+  const int jl = tid % kKeyChunk;
+  const int grp = tid / kKeyChunk;
+  const float inv_sqrt_d = 0.08838834764831845f;  // 1/sqrt(128)
+  for (int j0 = 0; j0 < g.nvk; j0 += kKeyChunk) {
+    __syncthreads();
+    for (int e = tid; e < kKeyChunk * (kHeadDim / 4); e += kRouteThreads) {
+      const int r = e / (kHeadDim / 4), c4 = e % (kHeadDim / 4);
+      const int j = j0 + r;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (j < g.nvk)
+        v = *reinterpret_cast<const float4*>(a.kc + (static_cast<size_t>(h) * g.nvk + j) * kHeadDim + 4 * c4);
+      float* dst = kcs + r * kKcStride + 4 * c4;
+      dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
+    }
+    __syncthreads();
+    float acc[QPT];
+#pragma unroll
+    for (int e = 0; e < QPT; ++e) acc[e] = 0.f;
+    const float* krow = kcs + jl * kKcStride;
+#pragma unroll 4
+    for (int d = 0; d < kHeadDim; ++d) {
+      const float kv = krow[d];
+      const float* qv = qcT + d * QB + grp * QPT;
+#pragma unroll
+      for (int e = 0; e < QPT; ++e) acc[e] = fmaf(qv[e], kv, acc[e]);
+    }
+    const int j = j0 + jl;
+    if (j < g.nvk) {
+#pragma unroll
+      for (int e = 0; e < QPT; ++e) sc[(grp * QPT + e) * g.nvk + j] = acc[e] * inv_sqrt_d;
+    }
+  }
+  __syncthreads();
+
+  if (a.scores != nullptr) {
+    for (int qi = 0; qi < QB; ++qi) {
+      const int i = i0 + qi;
+      if (i >= g.nq) break;
+      float* dst = a.scores + (static_cast<size_t>(h) * g.nq + i) * g.nvk;
+      for (int j = tid; j < g.nvk; j += kRouteThreads) dst[j] = sc[qi * g.nvk + j];
+    }
+  }
+
+  const int warp = tid / 32, lane = tid % 32;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int qi = warp; qi < QB; qi += kRouteThreads / 32) {
+    const int i = i0 + qi;
+    if (i >= g.nq) break;
+    const float* srow = sc + qi * g.nvk;
+    const int lo = max(0, i - g.R);
+    const int hi = min(g.nvk - 1, i + g.R);
+    const int nlv = max(0, hi - lo + 1);
+    const int ncand = g.nvk - nlv;
+    const int kp = min(g.K, ncand);
+    const bool take_all = (kp == ncand);
+    uint32_t tau = 0;
+    int need = 0;
+    if (!take_all) {
+      // Largest tau with #{candidates with key >= tau} >= kp, bit by bit.
+      for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t t = tau | (1u << bit);
+        int c = 0;
+        for (int j = lane; j < g.nvk; j += 32)
+          c += ((j < lo || j > hi) && order_key(srow[j]) >= t) ? 1 : 0;
+        c = __reduce_add_sync(0xFFFFFFFFu, c);
+        if (c >= kp) tau = t;
+      }
+      int gt = 0;
+      for (int j = lane; j < g.nvk; j += 32)
+        gt += ((j < lo || j > hi) && order_key(srow[j]) > tau) ? 1 : 0;
+      gt = __reduce_add_sync(0xFFFFFFFFu, gt);
+      need = kp - gt;
+    }
+    int32_t* out = a.idx + (static_cast<size_t>(h) * g.nq + i) * g.maxl;
+    int pos = 0, eq_seen = 0;
+    for (int j0 = 0; j0 < g.nblk; j0 += 32) {
+      const int j = j0 + lane;
+      bool sel = false, eq = false;
+      if (j < g.nvk) {
+        if (j >= lo && j <= hi) {
+          sel = true;
+        } else if (take_all) {
+          sel = true;
+        } else {
+          const uint32_t kk = order_key(srow[j]);
+          if (kk > tau) sel = true;
+          else if (kk == tau) eq = true;
+        }
+      } else if (j < g.nblk) {
+        sel = true;  // sink block
+      }
+      const unsigned eqm = __ballot_sync(0xFFFFFFFFu, eq);
+      if (eq) sel = (eq_seen + __popc(eqm & lt_mask)) < need;
+      eq_seen += __popc(eqm);
+      const unsigned sm = __ballot_sync(0xFFFFFFFFu, sel);
+      if (sel) out[pos + __popc(sm & lt_mask)] = j;
+      pos += __popc(sm);
+    }
+    for (int p = pos + lane; p < g.maxl; p += 32) out[p] = -1;
+    if (lane == 0) a.cnt[static_cast<size_t>(h) * g.nq + i] = pos;
+  }
+}
+
+int route_qb(const Geometry& g) {
+  if (g.nvk <= 1536) return 16;
+  if (g.nvk <= 3072) return 8;
+  return 4;
+}
+
+}  // namespace
+
+size_t route_topk_smem_bytes(const Geometry& g) {
+  const int qb = route_qb(g);
+  return sizeof(float) * (static_cast<size_t>(kHeadDim) * qb + kKeyChunk * kKcStride +
+                          static_cast<size_t>(qb) * g.nvk);
+}
+
+cudaError_t launch_pool(const PlanArgs& a, cudaStream_t s) {
+  const int nb = a.g.nq > a.g.nvk ? a.g.nq : a.g.nvk;
+  pool_kernel<<<dim3(nb, 2), 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_topk(const PlanArgs& a, cudaStream_t s) {
+  const int qb = route_qb(a.g);
+  const size_t smem = route_topk_smem_bytes(a.g);
+  const dim3 grid((a.g.nq + qb - 1) / qb, a.g.H);
+  cudaError_t e = cudaSuccess;
+  switch (qb) {
+    case 16:
+      e = cudaFuncSetAttribute(route_topk_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) route_topk_kernel<16><<<grid, kRouteThreads, smem, s>>>(a);
+      break;
+    case 8:
+      e = cudaFuncSetAttribute(route_topk_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) route_topk_kernel<8><<<grid, kRouteThreads, smem, s>>>(a);
+      break;
+    default:
+      e = cudaFuncSetAttribute(route_topk_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) route_topk_kernel<4><<<grid, kRouteThreads, smem, s>>>(a);
+      break;
+  }
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace sa
