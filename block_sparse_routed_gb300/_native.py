@@ -27,6 +27,7 @@ SA_TAIL_PAD = 1
 ENTRY_POINTS = (
     "sparse_attn_query",
     "sparse_attn_plan",
+    "sparse_attn_plan_static",
     "sparse_attn_fwd",
     "sparse_attn_last_device_status",
     "sparse_attn_status_string",
@@ -88,6 +89,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sparse_attn_query.restype = ctypes.c_int
     lib.sparse_attn_plan.argtypes = [P(SaParams), vp, vp, vp, vp, vp, vp, sz, vp]
     lib.sparse_attn_plan.restype = ctypes.c_int
+    lib.sparse_attn_plan_static.argtypes = [P(SaParams), vp, vp, vp, vp, vp, vp]
+    lib.sparse_attn_plan_static.restype = ctypes.c_int
     lib.sparse_attn_fwd.argtypes = [P(SaParams), vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.sparse_attn_fwd.restype = ctypes.c_int
     lib.sparse_attn_last_device_status.argtypes = [vp, vp, P(ctypes.c_int)]
@@ -117,6 +120,14 @@ def sparse_attn_plan(params, q, k, idx, cnt, route_scores, ws, ws_bytes, stream)
     """Raw call: device pointers as ints (0 for NULL).  Returns the status."""
     return load_library().sparse_attn_plan(
         ctypes.byref(params), q, k, idx, cnt, route_scores or None, ws, ws_bytes, stream or None
+    )
+
+
+def sparse_attn_plan_static(params, q, k, idx, cnt, route_scores, stream) -> int:
+    """Raw call of the no-allocation routing entry point (scratch in a fixed
+    device array inside the library).  Returns the status."""
+    return load_library().sparse_attn_plan_static(
+        ctypes.byref(params), q, k, idx, cnt, route_scores or None, stream or None
     )
 
 

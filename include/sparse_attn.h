@@ -32,8 +32,9 @@
  *
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers on the current CUDA device,
- *     owned by the caller, 16-byte aligned and contiguous.  The library
- *     allocates no device memory.
+ *     owned by the caller, 16-byte aligned and contiguous.  No entry point
+ *     allocates device memory (the one fixed scratch array of
+ *     sparse_attn_plan_static is part of the loaded library).
  *   - All GPU work is enqueued on `stream`; plan and fwd never synchronise
  *     the host.  Argument errors are returned before anything is enqueued.
  *   - A workspace `ws` of the size reported by sparse_attn_query belongs to
@@ -142,6 +143,31 @@ sa_status sparse_attn_plan(const sa_params* p, const void* q, const void* k, int
 sa_status sparse_attn_fwd(const sa_params* p, const void* q, const void* k, const void* v,
                           const float* key_bias, const int32_t* idx, const int32_t* cnt, void* o,
                           void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Routing without a caller workspace: the same computation and outputs as
+ * sparse_attn_plan, with its scratch (status word and block means) kept in a
+ * file-scope device array of SA_PLAN_STATIC_SCRATCH_BYTES instead of `ws`.
+ * The source pages have no counterpart to this entry point.  It is for
+ * callers that cannot give the library device scratch memory: plugins in a
+ * host application whose device memory belongs to the host's own pool
+ * allocator with no allocation hook for plugins, and code that must not call
+ * cudaMalloc because it synchronises the device.  It allocates nothing.
+ *   - Every GPU that loads the library holds the array until process exit.
+ *   - Problems whose plan workspace (sparse_attn_query's plan_ws_bytes)
+ *     exceeds SA_PLAN_STATIC_SCRATCH_BYTES return SA_EUNSUPPORTED before any
+ *     launch.  The five reference workloads need at most 25.2 MiB.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current (cudaGetSymbolAddress) and caches it; make that
+ *     first call before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents: calls
+ *     that overlap on the GPU (several streams or host threads) race, and the
+ *     caller must serialise them.  The status area is cleared on each call.
+ * Errors: as sparse_attn_plan (no workspace arguments).
+ */
+#define SA_PLAN_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+sa_status sparse_attn_plan_static(const sa_params* p, const void* q, const void* k, int32_t* idx,
+                                  int32_t* cnt, float* route_scores, cudaStream_t stream);
 
 /*
  * Reads the device status word of `ws` (written by the last plan or fwd
