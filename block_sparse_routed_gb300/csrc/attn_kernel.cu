@@ -97,6 +97,45 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Packed two-wide FP32 arithmetic and a three-input max (sm_100+ forms).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unf2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Max of 64 values: a depth-4 tree of three-input maxima.
+__device__ __forceinline__ float max64(const uint32_t (&s)[64]) {
+  float m[22];
+#pragma unroll
+  for (int i = 0; i < 21; ++i)
+    m[i] = fmax3(__uint_as_float(s[3 * i]), __uint_as_float(s[3 * i + 1]), __uint_as_float(s[3 * i + 2]));
+  m[21] = __uint_as_float(s[63]);
+  float n[8];
+#pragma unroll
+  for (int i = 0; i < 7; ++i) n[i] = fmax3(m[3 * i], m[3 * i + 1], m[3 * i + 2]);
+  n[7] = m[21];
+  return fmaxf(fmax3(n[0], n[1], n[2]), fmax3(n[3], n[4], fmax3(n[5], n[6], n[7])));
+}
+
 __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
   atomicCAS(status, 0, code);
 }
@@ -348,18 +387,32 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         tmem_ld32(tmem + lane_addr + kColS + 64u * b + 32, s1);
         tmem_wait_ld();
       }
-      const bool row_ok = (bits >> half) & 1;
+      const bool row_ok = (bits >> half) & 1;  // uniform across the warp
       const int nvalid = min(kBlock, g.T - blk * kBlock);
       const bool add_bias = (a.b2 != nullptr) && blk >= g.nvk;
-      const float* bb = add_bias ? a.b2 + static_cast<size_t>(blk) * kBlock : nullptr;
-      float mx = -INFINITY;
+      const bool fast = row_ok && nvalid == kBlock && !add_bias;
+      // Logit in log2 units: l = s * log2(e)/sqrt(128) + b2 (b2 = 0 off sinks).
+      // Both paths round identically where b2 = 0: the maximum of fma(s, c, 0)
+      // equals c * max(s), and p = 2^fma(s, c, b2 - m).
+      const float4* bb = add_bias ? reinterpret_cast<const float4*>(a.b2 + static_cast<size_t>(blk) * kBlock)
+                                  : nullptr;
+      float mx;
+      if (fast) {
+        mx = max64(s) * sl2;
+      } else {
+        mx = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < 64; ++k) {
-        float x = __uint_as_float(s[k]) * sl2;
-        if (add_bias && k < nvalid) x += __ldg(bb + k);
-        x = (row_ok && k < nvalid) ? x : -INFINITY;
-        s[k] = __float_as_uint(x);
-        mx = fmaxf(mx, x);
+        for (int q4 = 0; q4 < 16; ++q4) {
+          const float4 bv = add_bias ? __ldg(bb + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float bq[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int k = 4 * q4 + e;
+            const float bk = (k < nvalid) ? bq[e] : 0.f;
+            const float x = fmaf(__uint_as_float(s[k]), sl2, bk);
+            if (row_ok && k < nvalid) mx = fmaxf(mx, x);
+          }
+        }
       }
       const float m_new = fmaxf(m_run, mx);
       const bool resc = (m_run != -INFINITY) && (m_new > m_run + 8.0f);
@@ -389,16 +442,52 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
       }
       const float msub = (m_run == -INFINITY) ? 0.f : m_run;
-      float lsum = 0.f;
       uint32_t p[32];
+      uint64_t acc[4];
+      if (fast) {
+        // p = 2^(s * scale - m): one packed FMA per pair, one MUFU per value
+        const uint64_t sc2 = f2(sl2, sl2);
+        const uint64_t nm2 = f2(-msub, -msub);
 #pragma unroll
-      for (int k = 0; k < 64; k += 2) {
-        const float e0 = ex2_approx(__uint_as_float(s[k]) - msub);
-        const float e1 = ex2_approx(__uint_as_float(s[k + 1]) - msub);
-        lsum += e0 + e1;
-        p[k / 2] = pack_bf16x2(e0, e1);
+        for (int q = 0; q < 4; ++q) acc[q] = f2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 64; k += 2) {
+          float x0, x1;
+          unf2(ffma2(f2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), sc2, nm2), x0, x1);
+          const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+          acc[(k >> 1) & 3] = fadd2(acc[(k >> 1) & 3], f2(e0, e1));
+          p[k / 2] = pack_bf16x2(e0, e1);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[q] = f2(0.f, 0.f);
+        float e[64];
+#pragma unroll
+        for (int q4 = 0; q4 < 16; ++q4) {
+          const float4 bv = add_bias ? __ldg(bb + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float bq[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int k = 4 * q4 + t;
+            const float bk = (k < nvalid) ? bq[t] : 0.f;
+            const float x = fmaf(__uint_as_float(s[k]), sl2, bk - msub);
+            e[k] = (row_ok && k < nvalid) ? ex2_approx(x) : 0.f;
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 64; k += 2) {
+          acc[(k >> 1) & 3] = fadd2(acc[(k >> 1) & 3], f2(e[k], e[k + 1]));
+          p[k / 2] = pack_bf16x2(e[k], e[k + 1]);
+        }
       }
-      l_run += lsum;
+      {
+        float a0, a1, b0, b1, c0, c1, d0, d1;
+        unf2(acc[0], a0, a1);
+        unf2(acc[1], b0, b1);
+        unf2(acc[2], c0, c1);
+        unf2(acc[3], d0, d1);
+        l_run += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+      }
       tmem_st32(tmem + lane_addr + kColS + 64u * b, p);
       tmem_wait_st();
       tc_fence_before();

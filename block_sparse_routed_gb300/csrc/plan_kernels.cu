@@ -21,39 +21,42 @@ namespace {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// One CTA per (block, tensor): blockIdx.y = 0 pools Q over the nq query
-// blocks, 1 pools K over the nvk video key blocks.  Each thread owns 16-byte
-// column slices of a token row (8 dims of one head) and sums them down the
-// block's rows; consecutive threads read consecutive 16-byte slices, so every
-// row is read with full coalescing.  HBM-bound.
-__global__ void __launch_bounds__(256) pool_kernel(PlanArgs a) {
+// One CTA per (block, 256-slice column chunk, tensor): blockIdx.y = 0 pools
+// Q over the nq query blocks, 1 pools K over the nvk video key blocks.  Each
+// thread owns one 16-byte column slice of a token row (8 dims of one head)
+// and sums it down the block's rows; consecutive threads read consecutive
+// 16-byte slices, so every row is read with full coalescing.  HBM-bound.
+constexpr int kPoolThreads = 256;
+
+__global__ void __launch_bounds__(kPoolThreads) pool_kernel(PlanArgs a, int nchunks) {
   const Geometry& g = a.g;
   const bool isq = blockIdx.y == 0;
   const int nblocks = isq ? g.nq : g.nvk;
-  const int i = blockIdx.x;
+  const int i = blockIdx.x / nchunks;
+  const int chunk = blockIdx.x % nchunks;
   if (i >= nblocks) return;
   const int n = (i < g.nvk) ? kBlock : g.tail;  // the pad tail block owns `tail` rows
-  const uint4* src = reinterpret_cast<const uint4*>(isq ? a.q : a.k);
-  float* dst = isq ? a.qc : a.kc;
   const int vpr = g.H * (kHeadDim / 8);  // 16-byte slices per token row
-  const float fn = static_cast<float>(n);
-  for (int c = threadIdx.x; c < vpr; c += blockDim.x) {
-    const uint4* p = src + static_cast<size_t>(i) * kBlock * vpr + c;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-    for (int r = 0; r < n; ++r) {
-      const uint4 v = __ldg(p + static_cast<size_t>(r) * vpr);
-      acc[0] += bf16_lo(v.x); acc[1] += bf16_hi(v.x);
-      acc[2] += bf16_lo(v.y); acc[3] += bf16_hi(v.y);
-      acc[4] += bf16_lo(v.z); acc[5] += bf16_hi(v.z);
-      acc[6] += bf16_lo(v.w); acc[7] += bf16_hi(v.w);
-    }
-    const int h = c / (kHeadDim / 8);
-    const int d0 = (c % (kHeadDim / 8)) * 8;
-    float4* o = reinterpret_cast<float4*>(dst + (static_cast<size_t>(h) * nblocks + i) * kHeadDim + d0);
-    o[0] = make_float4(acc[0] / fn, acc[1] / fn, acc[2] / fn, acc[3] / fn);
-    o[1] = make_float4(acc[4] / fn, acc[5] / fn, acc[6] / fn, acc[7] / fn);
+  const int c = chunk * kPoolThreads + threadIdx.x;
+  if (c >= vpr) return;
+  const uint4* p = reinterpret_cast<const uint4*>(isq ? a.q : a.k) +
+                   static_cast<size_t>(i) * kBlock * vpr + c;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 16
+  for (int r = 0; r < n; ++r) {
+    const uint4 v = __ldg(p + static_cast<size_t>(r) * vpr);
+    acc[0] += bf16_lo(v.x); acc[1] += bf16_hi(v.x);
+    acc[2] += bf16_lo(v.y); acc[3] += bf16_hi(v.y);
+    acc[4] += bf16_lo(v.z); acc[5] += bf16_hi(v.z);
+    acc[6] += bf16_lo(v.w); acc[7] += bf16_hi(v.w);
   }
+  const float fn = static_cast<float>(n);
+  const int h = c / (kHeadDim / 8);
+  const int d0 = (c % (kHeadDim / 8)) * 8;
+  float* dst = isq ? a.qc : a.kc;
+  float4* o = reinterpret_cast<float4*>(dst + (static_cast<size_t>(h) * nblocks + i) * kHeadDim + d0);
+  o[0] = make_float4(acc[0] / fn, acc[1] / fn, acc[2] / fn, acc[3] / fn);
+  o[1] = make_float4(acc[4] / fn, acc[5] / fn, acc[6] / fn, acc[7] / fn);
 }
 
 // Order-preserving map of an FP32 score to an unsigned key; -0 and +0 map to
@@ -209,7 +212,9 @@ size_t route_topk_smem_bytes(const Geometry& g) {
 
 cudaError_t launch_pool(const PlanArgs& a, cudaStream_t s) {
   const int nb = a.g.nq > a.g.nvk ? a.g.nq : a.g.nvk;
-  pool_kernel<<<dim3(nb, 2), 256, 0, s>>>(a);
+  const int vpr = a.g.H * (kHeadDim / 8);
+  const int nchunks = (vpr + kPoolThreads - 1) / kPoolThreads;
+  pool_kernel<<<dim3(nb * nchunks, 2), kPoolThreads, 0, s>>>(a, nchunks);
   return cudaGetLastError();
 }
 
