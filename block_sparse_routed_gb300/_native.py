@@ -30,6 +30,7 @@ ENTRY_POINTS = (
     "sparse_attn_plan_static",
     "sparse_attn_fwd",
     "sparse_attn_last_device_status",
+    "sparse_attn_last_cuda_error",
     "sparse_attn_status_string",
 )
 
@@ -66,7 +67,11 @@ class SaSizes(ctypes.Structure):
 class SparseAttnError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = int(status)
-        super().__init__(f"{what}: {status_string(status)}")
+        msg = f"{what}: {status_string(status)}"
+        if self.status == SA_ECUDA:
+            code, text = sparse_attn_last_cuda_error()
+            msg += f" (CUDA error {code}: {text})"
+        super().__init__(msg)
 
 
 _lib = None
@@ -95,6 +100,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sparse_attn_fwd.restype = ctypes.c_int
     lib.sparse_attn_last_device_status.argtypes = [vp, vp, P(ctypes.c_int)]
     lib.sparse_attn_last_device_status.restype = ctypes.c_int
+    lib.sparse_attn_last_cuda_error.argtypes = [P(ctypes.c_char_p)]
+    lib.sparse_attn_last_cuda_error.restype = ctypes.c_int
     lib.sparse_attn_status_string.argtypes = [ctypes.c_int]
     lib.sparse_attn_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -144,6 +151,13 @@ def sparse_attn_last_device_status(ws, stream) -> int:
     if st != SA_OK:
         raise SparseAttnError(st, "sparse_attn_last_device_status")
     return out.value
+
+
+def sparse_attn_last_cuda_error():
+    """(code, message) of the last CUDA error behind an SA_ECUDA on this thread."""
+    msg = ctypes.c_char_p()
+    code = load_library().sparse_attn_last_cuda_error(ctypes.byref(msg))
+    return code, (msg.value or b"").decode()
 
 
 def sparse_attn_status_string(status: int) -> str:

@@ -17,6 +17,15 @@
 namespace {
 using namespace sa;
 
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+// Records a failed CUDA call for sparse_attn_last_cuda_error.
+bool cuda_failed(cudaError_t e) {
+  if (e == cudaSuccess) return false;
+  g_last_cuda_error = e;
+  return true;
+}
+
 constexpr uint64_t align256(uint64_t x) { return (x + 255u) & ~uint64_t(255); }
 
 sa_status derive(const sa_params* p, Geometry* g, sa_sizes* out) {
@@ -88,13 +97,13 @@ sa_status check_device() {
   static std::mutex mu;
   static signed char state[128] = {0};  // 0 unknown, 1 ok, -1 unsupported
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SA_ECUDA;
+  if (cuda_failed(cudaGetDevice(&dev))) return SA_ECUDA;
   if (dev < 0 || dev >= 128) return SA_EUNSUPPORTED;
   std::lock_guard<std::mutex> lock(mu);
   if (state[dev] == 0) {
     int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    if (cuda_failed(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) ||
+        cuda_failed(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)))
       return SA_ECUDA;
     state[dev] = (major == 10 && minor == 3) ? 1 : -1;
   }
@@ -163,9 +172,9 @@ SA_API sa_status sparse_attn_plan(const sa_params* p, const void* q, const void*
   a.cnt = cnt;
   a.scores = route_scores;
   a.g = g;
-  if (cudaMemsetAsync(ws, 0, kStatusBytes, stream) != cudaSuccess) return SA_ECUDA;
-  if (launch_pool(a, stream) != cudaSuccess) return SA_ECUDA;
-  if (launch_route_topk(a, stream) != cudaSuccess) return SA_ECUDA;
+  if (cuda_failed(cudaMemsetAsync(ws, 0, kStatusBytes, stream))) return SA_ECUDA;
+  if (cuda_failed(launch_pool(a, stream))) return SA_ECUDA;
+  if (cuda_failed(launch_route_topk(a, stream))) return SA_ECUDA;
   return SA_OK;
 }
 
@@ -192,8 +201,8 @@ SA_API sa_status sparse_attn_fwd(const sa_params* p, const void* q, const void* 
   uint8_t* w = static_cast<uint8_t*>(ws);
   int32_t* status = reinterpret_cast<int32_t*>(w);
   float* b2 = key_bias ? reinterpret_cast<float*>(w + kStatusBytes) : nullptr;
-  if (cudaMemsetAsync(ws, 0, kStatusBytes, stream) != cudaSuccess) return SA_ECUDA;
-  if (key_bias && launch_bias_prep(key_bias, b2, status, g, stream) != cudaSuccess) return SA_ECUDA;
+  if (cuda_failed(cudaMemsetAsync(ws, 0, kStatusBytes, stream))) return SA_ECUDA;
+  if (key_bias && cuda_failed(launch_bias_prep(key_bias, b2, status, g, stream))) return SA_ECUDA;
 
   AttnArgs a;
   a.idx = idx;
@@ -201,11 +210,12 @@ SA_API sa_status sparse_attn_fwd(const sa_params* p, const void* q, const void* 
   a.b2 = b2;
   a.o = static_cast<uint16_t*>(o);
   a.status = status;
+  a.unit_counter = status + 1;  // inside the status area, cleared above
   a.g = g;
   a.n_dense = (g.T - g.r0 + 127) / 128;
   a.n_pairs = (g.nq + 1) / 2;
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(128.0));
-  if (launch_attention(tq, tk, tv, a, stream) != cudaSuccess) return SA_ECUDA;
+  if (cuda_failed(launch_attention(tq, tk, tv, a, stream))) return SA_ECUDA;
   return SA_OK;
 }
 
@@ -213,11 +223,17 @@ SA_API sa_status sparse_attn_last_device_status(const void* ws, cudaStream_t str
                                                 sa_status* out) {
   if (!ws || !out) return SA_EINVAL;
   int32_t v = 0;
-  if (cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+  if (cuda_failed(cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, stream)))
     return SA_ECUDA;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return SA_ECUDA;
+  if (cuda_failed(cudaStreamSynchronize(stream))) return SA_ECUDA;
   *out = static_cast<sa_status>(v);
   return SA_OK;
+}
+
+SA_API int sparse_attn_last_cuda_error(const char** message) {
+  const cudaError_t e = g_last_cuda_error;
+  if (message) *message = cudaGetErrorString(e);
+  return static_cast<int>(e);
 }
 
 SA_API const char* sparse_attn_status_string(sa_status s) {

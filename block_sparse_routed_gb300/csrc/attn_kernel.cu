@@ -1,7 +1,7 @@
 // Exact attention over block lists, and dense attention over every key, for
-// sm_103a: TMA loads of 64-key K/V blocks into 128-byte-swizzled shared
-// memory, QK^T and PV on tcgen05 tensor cores with FP32 accumulators in
-// tensor memory, and an online base-2 softmax in registers.
+// sm_103a: TMA loads of K/V blocks into 128-byte-swizzled shared memory,
+// QK^T and PV on tcgen05 tensor cores with FP32 accumulators in tensor
+// memory, and an online base-2 softmax in registers.
 //
 // What is computed ("Sol-Attn and Spark for MiniMax-H3", "H3 pipeline
 // integration"; "Add key bias to chunked Sol-Attn producers", "Summary" and
@@ -12,20 +12,42 @@
 // natural-log units and converted once to log2 units, so the kernel works in
 // base 2 throughout: l2 = (q . k) * log2(e) / sqrt(128) + bias * log2(e).
 //
-// Work units (one CTA each, two CTAs per SM):
-//   * sparse: a pair of consecutive query blocks of one head (128 rows).  The
-//     CTA walks the sorted union of the two lists; a key block that is in
-//     only one list is masked to -inf for the other block's 64 rows.
+// Work units (128 query rows each, the M of one tcgen05.mma):
+//   * sparse: a pair of consecutive query blocks of one head.  The walk is
+//     the sorted union of the two lists; a key block that is in only one list
+//     is masked to -inf for the other block's 64 rows.
 //   * dense: 128 consecutive densely evaluated rows of one head, walking all
 //     key blocks.
-// Warp roles: warp 0 issues TMA loads, warp 1 owns tensor memory and issues
-// the MMAs (one thread), warps 2-5 run the softmax (thread = query row =
-// tensor-memory lane) and the epilogue.
+// The walk advances 128 keys (two entries) per step; an odd last entry is
+// paired with a masked copy of itself.
 //
-// Tensor memory (256 columns): O accumulator in columns [0, 128); two S
-// buffers of 64 FP32 columns at 128 and 192.  After the softmax has read S_j
-// it writes P_j as packed BF16 pairs into the first 32 columns of the same
-// buffer, and PV_j reads P_j from there (A operand in tensor memory).
+// The kernel is persistent: one CTA per SM takes units from a global counter
+// (dense units first, the longest).  A scheduler warp prepares the next unit
+// (list merge) while the current one runs, Q is double-buffered, and the K/V
+// ring, the S buffers and every barrier phase continue across units, so the
+// next unit's loads and first MMAs overlap the current unit's tail.
+//
+// Schedule.  A tcgen05.mma that accumulates into the same tensor-memory tile
+// as the instruction issued just before it stalls the issuing thread, while
+// alternating two independent accumulators keeps the tensor pipe full.  So in
+// phase g (a global step index) the MMA thread interleaves the K-steps of
+// PV_g (O += P_g V_g) and of S_{g+2} = Q K_{g+2}^T.  Three S buffers make that
+// possible; P_g is written as packed BF16 over the first 64 columns of S_g's
+// buffer.  S_{g+2} reuses the buffer of P_{g-1}, so it waits for PV_{g-1} to
+// complete; two K-steps of PV_g are issued before that wait to keep the pipe
+// busy.
+//
+// Warp roles (11 warps): warp 0 issues TMA loads (Q per unit; K and V per
+// step through a 4-slot ring), warp 1 owns tensor memory and issues the MMAs
+// (one thread), warps 2-5 (softmax group 0) and 6-9 (group 1) each own one
+// query row per thread (= tensor-memory lane); group 0 takes even global
+// steps and group 1 odd ones, all 128 columns each, so two steps' softmax run
+// at once.  The groups share one lazily updated reference maximum per row,
+// passed step to step through shared memory; each keeps a partial row sum;
+// both merge and store the output in the unit's epilogue.  Warp 10 schedules
+// units and merges their block lists.
+//
+// Tensor memory (512 columns): O in [0, 128); S buffers at 128, 256, 384.
 #include <cstdint>
 
 #include "internal.h"
@@ -34,44 +56,60 @@
 namespace sa {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kTmemCols = 256;
+constexpr int kThreads = 352;
+constexpr int kSoftmaxThreads = 256;  // warps 2..9
+constexpr int kTmemCols = 512;
 constexpr uint32_t kColO = 0;
-constexpr uint32_t kColS = 128;  // S buffer b at kColS + 64 b
+constexpr uint32_t kColS = 128;  // S buffer b at kColS + 128 b, b in {0, 1, 2}
+constexpr int kSlots = 4;        // K/V ring slots
+constexpr uint32_t kSlotBytes = 32768;  // K or V of 128 keys: 2 chunks x [128 rows x 128 B]
+constexpr uint32_t kQBytes = 32768;     // Q tile: 2 chunks x [128 rows x 128 B]
+constexpr float kRescaleLog2 = 32.0f;
 
 // Shared-memory layout (bytes from a 1024-aligned base).
-constexpr uint32_t kOffQ = 0;             // Q tile: 2 chunks x [128 rows x 128 B]
-constexpr uint32_t kOffK = 32768;         // K stage s: 2 chunks x [64 rows x 128 B]
-constexpr uint32_t kOffV = 65536;         // V stage s
-constexpr uint32_t kStageBytes = 16384;   // one 64-key block of K (or V)
-constexpr uint32_t kOffEnt = 98304;       // union list entries (int32)
 constexpr int kMaxEnt = 2 * kMaxList;
-constexpr uint32_t kOffBar = kOffEnt + 4 * kMaxEnt;
-constexpr uint32_t kOffMisc = kOffBar + 256;
+constexpr uint32_t kOffQ = 0;                                   // 2 Q buffers
+constexpr uint32_t kOffRing = 2 * kQBytes;                      // kSlots x kSlotBytes
+constexpr uint32_t kOffEnt = kOffRing + kSlots * kSlotBytes;    // 2 x kMaxEnt int32
+constexpr uint32_t kOffScratch = kOffEnt + 2 * 4 * kMaxEnt;     // 2 x kMaxList int32 (merge)
+constexpr uint32_t kOffXchg = kOffScratch + 2 * 4 * kMaxList;   // [3][128] refs + [2][128] sums
+constexpr uint32_t kOffUnit = kOffXchg + 4 * 5 * 128;           // 2 unit descriptors
+constexpr uint32_t kOffBar = kOffUnit + 64;
+constexpr uint32_t kOffMisc = kOffBar + 512;
 constexpr uint32_t kSmemUsed = kOffMisc + 64;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // alignment slack
-
-// Merge scratch lives in the V stages, which are untouched until the list is
-// ready.
-constexpr uint32_t kOffListA = kOffV;
-constexpr uint32_t kOffListB = kOffV + 4 * kMaxList;
-constexpr uint32_t kOffMerged = kOffV + 8 * kMaxList;
-static_assert(kOffMerged + 4 * kMaxEnt <= kOffEnt, "merge scratch must fit in the V stages");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // Barrier indices (8 bytes each).
 enum {
-  BAR_Q = 0,
-  BAR_KFULL = 1,   // +s
-  BAR_VFULL = 3,   // +s
-  BAR_KEMPTY = 5,  // +s
-  BAR_VEMPTY = 7,  // +s
-  BAR_SFULL = 9,   // +b
-  BAR_PFULL = 11,  // +b
-  BAR_PVDONE = 13, // +b
-  BAR_OFULL = 15,
-  BAR_DRAIN = 16,
-  NUM_BARS = 17
+  BAR_QFULL = 0,     // +slot (2): Q tile landed
+  BAR_QEMPTY = 2,    // +slot: the unit's last S MMA completed
+  BAR_FULL = 4,      // +ring slot (4)
+  BAR_EMPTY = 8,     // +ring slot
+  BAR_SFULL = 12,    // +buffer (3)
+  BAR_PFULL = 15,    // +buffer
+  BAR_PVDONE = 18,   // +buffer
+  BAR_MREADY = 21,   // +buffer: reference of that step published
+  BAR_OFULL = 24,    // the unit's last PV completed
+  BAR_OEMPTY = 25,   // the epilogue has read O
+  BAR_UFULL = 26,    // +slot (2): unit descriptor ready
+  BAR_UEMPTY = 28,   // +slot: every role is done with the descriptor
+  BAR_DRAIN = 30,
+  NUM_BARS = 31
 };
+static_assert(NUM_BARS * 8 <= 512, "barrier area");
+
+struct UnitDesc {
+  int32_t valid;  // 0 marks the end of the work
+  int32_t h;
+  int32_t row0;
+  int32_t iA;
+  int32_t iB;     // -1 when the pair has one block
+  int32_t dense;
+  int32_t n_ent;  // list entries (dense: all key blocks)
+  int32_t pad;
+};
+static_assert(sizeof(UnitDesc) * 2 <= 64, "unit area");
 
 constexpr uint32_t kEntMaskShift = 30;
 constexpr uint32_t kEntBlockMask = (1u << kEntMaskShift) - 1u;
@@ -93,8 +131,21 @@ __device__ __forceinline__ int upper_bound_s(const int32_t* a, int n, int32_t x)
   return lo;
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+// Barrier over `n` threads that also returns the OR of `pred` across them,
+// so that a failure seen by any thread is acted on by all of them together.
+__device__ __forceinline__ bool named_bar_or(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
+  atomicCAS(status, 0, code);
 }
 
 // Packed two-wide FP32 arithmetic and a three-input max (sm_100+ forms).
@@ -136,11 +187,33 @@ __device__ __forceinline__ float max64(const uint32_t (&s)[64]) {
   return fmaxf(fmax3(n[0], n[1], n[2]), fmax3(n[3], n[4], fmax3(n[5], n[6], n[7])));
 }
 
-__device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
-  atomicCAS(status, 0, code);
+// Work unit u: dense tiles first (they are the longest), then the sparse
+// query-block pairs, head-major.
+__device__ __forceinline__ void decode_unit(const AttnArgs& a, int u, UnitDesc& d) {
+  const Geometry& g = a.g;
+  const int units_dense = g.H * a.n_dense;
+  d.valid = 1;
+  d.pad = 0;
+  if (u < units_dense) {
+    d.dense = 1;
+    d.h = u / a.n_dense;
+    d.row0 = g.r0 + 128 * (u % a.n_dense);
+    d.iA = 0;
+    d.iB = -1;
+    d.n_ent = g.nblk;
+  } else {
+    const int v = u - units_dense;
+    d.dense = 0;
+    d.h = v / a.n_pairs;
+    const int p = v % a.n_pairs;
+    d.iA = 2 * p;
+    d.iB = (2 * p + 1 < g.nq) ? 2 * p + 1 : -1;
+    d.row0 = kBlock * d.iA;
+    d.n_ent = 0;
+  }
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
 attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
   const Geometry& g = a.g;
@@ -148,211 +221,293 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(base);
-  int32_t* ent = reinterpret_cast<int32_t*>(base + kOffEnt);
+  float* xchg = reinterpret_cast<float*>(base + kOffXchg);
+  UnitDesc* udesc = reinterpret_cast<UnitDesc*>(base + kOffUnit);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(base + kOffMisc);
-  volatile int32_t* s_nent = reinterpret_cast<volatile int32_t*>(base + kOffMisc + 8);
   volatile int32_t* s_abort = reinterpret_cast<volatile int32_t*>(base + kOffMisc + 16);
   volatile int32_t* s_status = reinterpret_cast<volatile int32_t*>(base + kOffMisc + 24);
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * i; };
+  auto ent_buf = [&](int slot) { return reinterpret_cast<int32_t*>(base + kOffEnt + 4u * kMaxEnt * slot); };
 
   if (threadIdx.x == 0) {
     *s_status = *reinterpret_cast<volatile int32_t*>(a.status);
     *s_abort = 0;
-    *s_nent = 0;
   }
   __syncthreads();
   if (*s_status != 0) return;  // an earlier step on this stream failed
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-
-  // ---- which unit
-  const int units_dense = g.H * a.n_dense;
-  const bool dense = static_cast<int>(blockIdx.x) < units_dense;
-  int h, row0, iA = 0, iB = -1;
-  if (dense) {
-    h = blockIdx.x / a.n_dense;
-    row0 = g.r0 + 128 * (blockIdx.x % a.n_dense);
-  } else {
-    const int v = blockIdx.x - units_dense;
-    h = v / a.n_pairs;
-    const int p = v % a.n_pairs;
-    iA = 2 * p;
-    iB = (2 * p + 1 < g.nq) ? 2 * p + 1 : -1;
-    row0 = kBlock * iA;
-  }
+  const int total_units = g.H * (a.n_dense + a.n_pairs);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NUM_BARS; ++i) mbar_init(bar(i), 1);
-    mbar_init(bar(BAR_PFULL + 0), 4);
-    mbar_init(bar(BAR_PFULL + 1), 4);
-    if (dense) *s_nent = g.nblk;
+    for (int b = 0; b < 3; ++b) mbar_init(bar(BAR_PFULL + b), 4);   // the owning group's 4 warps
+    for (int b = 0; b < 3; ++b) mbar_init(bar(BAR_MREADY + b), 4);
+    mbar_init(bar(BAR_OEMPTY), 8);                                   // all softmax warps
+    for (int s = 0; s < 2; ++s) mbar_init(bar(BAR_UEMPTY + s), 10);  // producer + MMA + 8 softmax
     fence_barrier_init();
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tslot), kTmemCols);
     tmem_relinquish();
   }
-
-  // ---- union of the two block lists (sparse units), warps 2..5
-  if (!dense && warp >= 2) {
-    const int t2 = threadIdx.x - 64;
-    int32_t* la = reinterpret_cast<int32_t*>(base + kOffListA);
-    int32_t* lb = reinterpret_cast<int32_t*>(base + kOffListB);
-    int32_t* mg = reinterpret_cast<int32_t*>(base + kOffMerged);
-    const int nA = a.cnt[static_cast<size_t>(h) * g.nq + iA];
-    const int nB = (iB >= 0) ? a.cnt[static_cast<size_t>(h) * g.nq + iB] : 0;
-    const bool bad_cnt = nA < 1 || nA > g.maxl || nB < 0 || nB > g.maxl;
-    if (!bad_cnt) {
-      const int32_t* ga = a.idx + (static_cast<size_t>(h) * g.nq + iA) * g.maxl;
-      for (int k = t2; k < nA; k += 128) la[k] = ga[k];
-      if (iB >= 0) {
-        const int32_t* gb = a.idx + (static_cast<size_t>(h) * g.nq + iB) * g.maxl;
-        for (int k = t2; k < nB; k += 128) lb[k] = gb[k];
-      }
-    }
-    named_bar_sync(1, 128);
-    // validate: ascending, in range
-    bool bad = bad_cnt;
-    if (!bad_cnt) {
-      for (int k = t2; k < nA; k += 128)
-        bad |= la[k] < 0 || la[k] >= g.nblk || (k + 1 < nA && la[k] >= la[k + 1]);
-      for (int k = t2; k < nB; k += 128)
-        bad |= lb[k] < 0 || lb[k] >= g.nblk || (k + 1 < nB && lb[k] >= lb[k + 1]);
-    }
-    if (bad) *s_abort = 1;
-    named_bar_sync(1, 128);
-    if (*s_abort == 0) {
-      // stable merge with duplicates: A before an equal B
-      for (int k = t2; k < nA; k += 128)
-        mg[k + lower_bound_s(lb, nB, la[k])] = la[k] | (1 << kEntMaskShift);
-      for (int k = t2; k < nB; k += 128)
-        mg[k + upper_bound_s(la, nA, lb[k])] = lb[k] | (2 << kEntMaskShift);
-      named_bar_sync(1, 128);
-      if (warp == 2) {
-        const int n = nA + nB;
-        int pos = 0;
-        for (int m0 = 0; m0 < n; m0 += 32) {
-          const int m = m0 + lane;
-          bool keep = false;
-          int32_t val = 0;
-          if (m < n) {
-            const int32_t cur = mg[m];
-            const int32_t blk = cur & kEntBlockMask;
-            const bool dup_of_prev = m > 0 && (mg[m - 1] & kEntBlockMask) == blk;
-            const bool next_same = m + 1 < n && (mg[m + 1] & kEntBlockMask) == blk;
-            keep = !dup_of_prev;
-            val = next_same ? (blk | (3 << kEntMaskShift)) : cur;
-          }
-          const unsigned km = __ballot_sync(0xFFFFFFFFu, keep);
-          if (keep) ent[pos + __popc(km & ((1u << lane) - 1u))] = val;
-          pos += __popc(km);
-        }
-        if (lane == 0) *s_nent = pos;
-      }
-    }
-  }
-
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  if (*s_abort != 0) {
-    if (threadIdx.x == 0) set_status(a.status, 1 /* SA_EINVAL */);
-    __syncthreads();
-    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
-    return;
-  }
-  const int n = *s_nent;
-  const uint32_t sQ = sbase + kOffQ;
 
-  if (warp == 0) {
+  // Entry e of unit `d` (descriptor slot `slot`): block index and row-half
+  // mask (bit 0: rows 0-63, bit 1: rows 64-127).  An odd count is padded with
+  // a masked copy of the last entry so every step loads two real blocks.
+  auto entry = [&](const UnitDesc& d, int slot, int e, int& blk, int& bits) {
+    const bool pad = e >= d.n_ent;
+    const int ee = pad ? d.n_ent - 1 : e;
+    if (d.dense) {
+      blk = ee;
+      bits = 3;
+    } else {
+      const int32_t v = ent_buf(slot)[ee];
+      blk = static_cast<int>(static_cast<uint32_t>(v) & kEntBlockMask);
+      bits = static_cast<int>(static_cast<uint32_t>(v) >> kEntMaskShift);
+    }
+    if (pad) bits = 0;
+  };
+  // Waits for unit k's descriptor; false when waiting failed.
+  auto wait_unit = [&](int k) -> bool {
+    return mbar_wait(bar(BAR_UFULL + (k & 1)), (k >> 1) & 1, kWaitLimitNs);
+  };
+
+  if (warp == 10) {
+    // ------------------------------------------------------------ scheduler
+    int32_t* la = reinterpret_cast<int32_t*>(base + kOffScratch);
+    int32_t* lb = la + kMaxList;
+    for (int k = 0;; ++k) {
+      const int slot = k & 1;
+      bool ok = true;
+      if (k >= 2) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_UEMPTY + slot), ((k - 2) >> 1) & 1, kWaitLimitNs));
+      if (!ok || *s_abort) {
+        *s_abort = 1;
+        set_status(a.status, 5 /* SA_ETIMEOUT */);
+        break;
+      }
+      int u = 0;
+      if (lane == 0) u = atomicAdd(a.unit_counter, 1);
+      u = __shfl_sync(0xFFFFFFFFu, u, 0);
+      UnitDesc d;
+      bool bad = false;
+      if (u >= total_units) {
+        d.valid = 0;
+      } else {
+        decode_unit(a, u, d);
+        if (!d.dense) {
+          const int nA = a.cnt[static_cast<size_t>(d.h) * g.nq + d.iA];
+          const int nB = (d.iB >= 0) ? a.cnt[static_cast<size_t>(d.h) * g.nq + d.iB] : 0;
+          bad = nA < 1 || nA > g.maxl || nB < 0 || nB > g.maxl;
+          if (!bad) {
+            const int32_t* ga = a.idx + (static_cast<size_t>(d.h) * g.nq + d.iA) * g.maxl;
+            for (int k2 = lane; k2 < nA; k2 += 32) la[k2] = ga[k2];
+            if (d.iB >= 0) {
+              const int32_t* gb = a.idx + (static_cast<size_t>(d.h) * g.nq + d.iB) * g.maxl;
+              for (int k2 = lane; k2 < nB; k2 += 32) lb[k2] = gb[k2];
+            }
+            __syncwarp();
+            for (int k2 = lane; k2 < nA; k2 += 32)
+              bad |= la[k2] < 0 || la[k2] >= g.nblk || (k2 + 1 < nA && la[k2] >= la[k2 + 1]);
+            for (int k2 = lane; k2 < nB; k2 += 32)
+              bad |= lb[k2] < 0 || lb[k2] >= g.nblk || (k2 + 1 < nB && lb[k2] >= lb[k2 + 1]);
+          }
+          bad = __any_sync(0xFFFFFFFFu, bad);
+          if (!bad) {
+            // stable merge with duplicates (A before an equal B), then drop
+            // the second copy of each duplicated block and mark it for both
+            int32_t* mg = ent_buf(slot);
+            for (int k2 = lane; k2 < nA; k2 += 32)
+              mg[k2 + lower_bound_s(lb, nB, la[k2])] = static_cast<int32_t>(la[k2] | (1u << kEntMaskShift));
+            for (int k2 = lane; k2 < nB; k2 += 32)
+              mg[k2 + upper_bound_s(la, nA, lb[k2])] = static_cast<int32_t>(lb[k2] | (2u << kEntMaskShift));
+            __syncwarp();
+            const int nm = nA + nB;
+            int pos = 0;
+            int32_t prev_blk = -1;  // block of the element before this chunk
+            for (int m0 = 0; m0 < nm; m0 += 32) {
+              const int m = m0 + lane;
+              int32_t cur = 0, nxt = -1;
+              if (m < nm) cur = mg[m];
+              if (m + 1 < nm) nxt = mg[m + 1] & kEntBlockMask;
+              const int32_t blk = (m < nm) ? (cur & kEntBlockMask) : -2;
+              int32_t before = __shfl_up_sync(0xFFFFFFFFu, blk, 1);
+              if (lane == 0) before = prev_blk;
+              const bool keep = m < nm && blk != before;
+              const int32_t val = (nxt == blk) ? static_cast<int32_t>(blk | (3u << kEntMaskShift)) : cur;
+              prev_blk = __shfl_sync(0xFFFFFFFFu, blk, 31);
+              const unsigned km = __ballot_sync(0xFFFFFFFFu, keep);
+              __syncwarp();  // all reads of this chunk precede its writes
+              if (keep) mg[pos + __popc(km & ((1u << lane) - 1u))] = val;
+              pos += __popc(km);
+              __syncwarp();
+            }
+            d.n_ent = pos;
+          }
+        }
+      }
+      if (bad) {
+        if (lane == 0) set_status(a.status, 1 /* SA_EINVAL */);
+        *s_abort = 1;
+        d.valid = 0;
+      }
+      if (lane == 0) udesc[slot] = d;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_UFULL + slot));
+      if (!d.valid) break;
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      const int xq = h * kHeadDim;
-      mbar_arrive_expect_tx(bar(BAR_Q), 2 * 16384);
-      tma_load_2d(sQ, &tm_q, bar(BAR_Q), xq, row0);
-      tma_load_2d(sQ + 16384, &tm_q, bar(BAR_Q), xq + 64, row0);
-      int issued_k = 0, issued_v = 0;
+      int seq = 0;
       bool ok = true;
-      for (int j = 0; j < n && ok; ++j) {
-        const int s = j & 1;
-        const uint32_t par = ((j >> 1) & 1) ^ 1;
-        const int blk = dense ? j : (ent[j] & kEntBlockMask);
-        const int y = blk * kBlock;
-        if (!mbar_wait(bar(BAR_KEMPTY + s), par, kWaitLimitNs)) { ok = false; break; }
-        const uint32_t sK = sbase + kOffK + s * kStageBytes;
-        mbar_arrive_expect_tx(bar(BAR_KFULL + s), kStageBytes);
-        tma_load_2d(sK, &tm_k, bar(BAR_KFULL + s), xq, y);
-        tma_load_2d(sK + 8192, &tm_k, bar(BAR_KFULL + s), xq + 64, y);
-        issued_k = j + 1;
-        if (!mbar_wait(bar(BAR_VEMPTY + s), par, kWaitLimitNs)) { ok = false; break; }
-        const uint32_t sV = sbase + kOffV + s * kStageBytes;
-        mbar_arrive_expect_tx(bar(BAR_VFULL + s), kStageBytes);
-        tma_load_2d(sV, &tm_v, bar(BAR_VFULL + s), xq, y);
-        tma_load_2d(sV + 8192, &tm_v, bar(BAR_VFULL + s), xq + 64, y);
-        issued_v = j + 1;
-        if (*s_abort) { ok = false; break; }
+      for (int k = 0; ok; ++k) {
+        const int slot = k & 1;
+        if (!wait_unit(k)) { ok = false; break; }
+        const UnitDesc d = udesc[slot];
+        if (!d.valid) break;
+        const int n = (d.n_ent + 1) / 2;
+        const int xq = d.h * kHeadDim;
+        if (k >= 2 && !mbar_wait(bar(BAR_QEMPTY + slot), ((k - 2) >> 1) & 1, kWaitLimitNs)) { ok = false; break; }
+        const uint32_t sQ = sbase + kOffQ + slot * kQBytes;
+        mbar_arrive_expect_tx(bar(BAR_QFULL + slot), kQBytes);
+        tma_load_2d(sQ, &tm_q, bar(BAR_QFULL + slot), xq, d.row0);
+        tma_load_2d(sQ + 16384, &tm_q, bar(BAR_QFULL + slot), xq + 64, d.row0);
+        // Load order (the MMA thread consumes in the same order): K0, K1,
+        // then per step j: V_j, K_{j+2}.
+        auto load = [&](const CUtensorMap* map, int step) -> bool {
+          const int s = seq % kSlots;
+          const uint32_t par = ((seq / kSlots) & 1) ^ 1;
+          if (!mbar_wait(bar(BAR_EMPTY + s), par, kWaitLimitNs)) return false;
+          const uint32_t dst = sbase + kOffRing + s * kSlotBytes;
+          mbar_arrive_expect_tx(bar(BAR_FULL + s), kSlotBytes);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            int blk, bits;
+            entry(d, slot, 2 * step + hh, blk, bits);
+            tma_load_2d(dst + hh * 8192, map, bar(BAR_FULL + s), xq, blk * kBlock);
+            tma_load_2d(dst + 16384 + hh * 8192, map, bar(BAR_FULL + s), xq + 64, blk * kBlock);
+          }
+          ++seq;
+          return true;
+        };
+        ok = load(&tm_k, 0);
+        if (ok && n > 1) ok = load(&tm_k, 1);
+        for (int j = 0; j < n && ok; ++j) {
+          ok = load(&tm_v, j);
+          if (ok && j + 2 < n) ok = load(&tm_k, j + 2);
+          if (*s_abort) ok = false;
+        }
+        if (ok) mbar_arrive(bar(BAR_UEMPTY + slot));
       }
       if (!ok) {
         *s_abort = 1;
         set_status(a.status, 5 /* SA_ETIMEOUT */);
         // let copies in flight land before the CTA exits (bounded)
-        for (int j = max(0, issued_k - 2); j < issued_k; ++j)
-          mbar_wait(bar(BAR_KFULL + (j & 1)), (j >> 1) & 1, kWaitLimitNs);
-        for (int j = max(0, issued_v - 2); j < issued_v; ++j)
-          mbar_wait(bar(BAR_VFULL + (j & 1)), (j >> 1) & 1, kWaitLimitNs);
+        for (int q = max(0, seq - kSlots); q < seq; ++q)
+          mbar_wait(bar(BAR_FULL + q % kSlots), (q / kSlots) & 1, kWaitLimitNs);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t id_s = idesc_bf16(128, 64, false, false);   // S = Q K^T, both K-major
+      const uint32_t id_s = idesc_bf16(128, 128, false, false);  // S = Q K^T, both K-major
       const uint32_t id_o = idesc_bf16(128, 128, false, true);   // O += P V, V is MN-major
-      bool ok = mbar_wait(bar(BAR_Q), 0, kWaitLimitNs);
-      tc_fence_after();
-      auto issue_pv = [&](int jj) -> bool {
-        const int b = jj & 1;
-        const uint32_t par = (jj >> 1) & 1;
-        if (!mbar_wait(bar(BAR_PFULL + b), par, kWaitLimitNs)) return false;
-        if (!mbar_wait(bar(BAR_VFULL + b), par, kWaitLimitNs)) return false;
-        tc_fence_after();
-        const uint32_t sV = sbase + kOffV + b * kStageBytes;
-        const uint32_t pcol = tmem + kColS + 64u * b;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t bd = sdesc_sw128(sV + kk * 2048, 8192, 1024);
-          umma_ts(tmem + kColO, pcol + kk * 8, bd, id_o, (jj > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(bar(BAR_VEMPTY + b));
-        umma_commit(bar(BAR_PVDONE + b));
-        return true;
+      // A descriptor's start address is its low 14 bits (16-byte units):
+      // stepping through a tile is one add of a compile-time offset.
+      auto kmaj_off = [](int kk) { return static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4); };
+      auto vmaj_off = [](int kk) { return static_cast<uint64_t>((kk * 2048) >> 4); };
+      auto slot_addr = [&](int q) { return sbase + kOffRing + (q % kSlots) * kSlotBytes; };
+      auto wait_full = [&](int q) { return mbar_wait(bar(BAR_FULL + q % kSlots), (q / kSlots) & 1, kWaitLimitNs); };
+      auto s_col = [&](int gs) { return tmem + kColS + 128u * (gs % 3); };
+      // S_x reuses the buffer of P_{x-3}: PV_{x-3} must have completed.
+      auto wait_buffer_free = [&](int x) {
+        return x < 3 || mbar_wait(bar(BAR_PVDONE + (x - 3) % 3), ((x - 3) / 3) & 1, kWaitLimitNs);
       };
-      for (int j = 0; j < n && ok; ++j) {
-        const int b = j & 1;
-        const uint32_t par = (j >> 1) & 1;
-        if (!mbar_wait(bar(BAR_KFULL + b), par, kWaitLimitNs)) { ok = false; break; }
-        if (j >= 2 && !mbar_wait(bar(BAR_PVDONE + b), par ^ 1, kWaitLimitNs)) { ok = false; break; }
+      int seq = 0, G = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int slot = k & 1;
+        if (!wait_unit(k)) { ok = false; break; }
+        const UnitDesc d = udesc[slot];
+        if (!d.valid) break;
+        const int n = (d.n_ent + 1) / 2;
+        if (!mbar_wait(bar(BAR_QFULL + slot), (k >> 1) & 1, kWaitLimitNs)) { ok = false; break; }
+        const uint64_t q_base = sdesc_sw128(sbase + kOffQ + slot * kQBytes, 16, 1024);
+        // prologue: S_G (and S_{G+1}), interleaved
+        const int q0 = seq++;
+        const int q1 = n > 1 ? seq++ : -1;
+        ok = wait_full(q0) && wait_buffer_free(G) && (q1 < 0 || (wait_full(q1) && wait_buffer_free(G + 1)));
+        if (!ok) break;
         tc_fence_after();
-        const uint32_t sK = sbase + kOffK + b * kStageBytes;
-        const uint32_t scol = tmem + kColS + 64u * b;
+        {
+          const uint64_t k0 = sdesc_sw128(slot_addr(q0), 16, 1024);
+          const uint64_t k1 = q1 >= 0 ? sdesc_sw128(slot_addr(q1), 16, 1024) : 0;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = sdesc_sw128(sQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sK + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-          umma_ss(scol, ad, bd, id_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) {
+            umma_ss(s_col(G), q_base + kmaj_off(kk), k0 + kmaj_off(kk), id_s, kk > 0 ? 1u : 0u);
+            if (q1 >= 0) umma_ss(s_col(G + 1), q_base + kmaj_off(kk), k1 + kmaj_off(kk), id_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(bar(BAR_EMPTY + q0 % kSlots));
+          umma_commit(bar(BAR_SFULL + G % 3));
+          if (q1 >= 0) {
+            umma_commit(bar(BAR_EMPTY + q1 % kSlots));
+            umma_commit(bar(BAR_SFULL + (G + 1) % 3));
+          }
+          if (n <= 2) umma_commit(bar(BAR_QEMPTY + slot));  // the unit's last S MMA
         }
-        umma_commit(bar(BAR_KEMPTY + b));
-        umma_commit(bar(BAR_SFULL + b));
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
-        if (*s_abort) { ok = false; break; }
-      }
-      if (ok && n > 0) ok = issue_pv(n - 1);
-      if (ok) {
+        for (int j = 0; j < n && ok; ++j) {
+          const int gs = G + j;
+          const int qv = seq++;
+          const bool has_k = j + 2 < n;
+          const int qk = has_k ? seq++ : -1;
+          if (!wait_full(qv)) { ok = false; break; }
+          if (!mbar_wait(bar(BAR_PFULL + gs % 3), (gs / 3) & 1, kWaitLimitNs)) { ok = false; break; }
+          // The unit's first PV overwrites O: the previous epilogue must be done.
+          if (j == 0 && k >= 1 && !mbar_wait(bar(BAR_OEMPTY), (k - 1) & 1, kWaitLimitNs)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t vs = sdesc_sw128(slot_addr(qv), 16384, 1024);
+          const uint32_t pcol = s_col(gs);
+          // Two K-steps of PV first keep the pipe busy while PV_{g-1} drains.
+          umma_ts(tmem + kColO, pcol, vs + vmaj_off(0), id_o, j > 0 ? 1u : 0u);
+          umma_ts(tmem + kColO, pcol + 8, vs + vmaj_off(1), id_o, 1u);
+          if (has_k) {
+            if (!wait_full(qk) || !wait_buffer_free(gs + 2)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t ks = sdesc_sw128(slot_addr(qk), 16, 1024);
+            const uint32_t scol = s_col(gs + 2);
+            // S_{g+2} and the rest of PV_g alternate: two accumulators in flight.
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              umma_ss(scol, q_base + kmaj_off(kk), ks + kmaj_off(kk), id_s, kk > 0 ? 1u : 0u);
+              if (kk < 6) umma_ts(tmem + kColO, pcol + (kk + 2) * 8, vs + vmaj_off(kk + 2), id_o, 1u);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 2; kk < 8; ++kk) umma_ts(tmem + kColO, pcol + kk * 8, vs + vmaj_off(kk), id_o, 1u);
+          }
+          umma_commit(bar(BAR_EMPTY + qv % kSlots));
+          umma_commit(bar(BAR_PVDONE + gs % 3));
+          if (has_k) {
+            umma_commit(bar(BAR_EMPTY + qk % kSlots));
+            umma_commit(bar(BAR_SFULL + (gs + 2) % 3));
+            if (j + 2 == n - 1) umma_commit(bar(BAR_QEMPTY + slot));  // the unit's last S MMA
+          }
+          if (*s_abort) { ok = false; break; }
+        }
+        if (!ok) break;
         umma_commit(bar(BAR_OFULL));
-      } else {
+        mbar_arrive(bar(BAR_UEMPTY + slot));
+        G += n;
+      }
+      if (!ok) {
         *s_abort = 1;
         set_status(a.status, 5 /* SA_ETIMEOUT */);
         umma_commit(bar(BAR_DRAIN));
@@ -361,165 +516,218 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
   } else {
     // ------------------------------------------------------------ softmax
+    const int grp = (warp - 2) / 4;        // owns global steps with parity grp
     const int quad = warp & 3;             // tensor-memory lane quarter of this warp
     const int row = quad * 32 + lane;      // query row within the tile
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const int half = row >> 6;
     const float sl2 = a.scale_log2;
-    float m_run = -INFINITY, l_run = 0.f;
+    float* rref = xchg;                    // [3][128]: reference after step g at g % 3
+    float* xl = xchg + 3 * 128;            // [2][128]: partial row sums
+    int G = 0;
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      const int b = j & 1;
-      const uint32_t par = (j >> 1) & 1;
-      int blk, bits;
-      if (dense) { blk = j; bits = 3; }
-      else { const int32_t e = ent[j]; blk = e & kEntBlockMask; bits = (e >> kEntMaskShift) & 3; }
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_SFULL + b), par, kWaitLimitNs))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t s[64];
-      {
-        uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
-        uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
-        tmem_ld32(tmem + lane_addr + kColS + 64u * b, s0);
-        tmem_ld32(tmem + lane_addr + kColS + 64u * b + 32, s1);
-        tmem_wait_ld();
-      }
-      const bool row_ok = (bits >> half) & 1;  // uniform across the warp
-      const int nvalid = min(kBlock, g.T - blk * kBlock);
-      const bool add_bias = (a.b2 != nullptr) && blk >= g.nvk;
-      const bool fast = row_ok && nvalid == kBlock && !add_bias;
-      // Logit in log2 units: l = s * log2(e)/sqrt(128) + b2 (b2 = 0 off sinks).
-      // Both paths round identically where b2 = 0: the maximum of fma(s, c, 0)
-      // equals c * max(s), and p = 2^fma(s, c, b2 - m).
-      const float4* bb = add_bias ? reinterpret_cast<const float4*>(a.b2 + static_cast<size_t>(blk) * kBlock)
-                                  : nullptr;
-      float mx;
-      if (fast) {
-        mx = max64(s) * sl2;
-      } else {
-        mx = -INFINITY;
+    for (int k = 0; ok; ++k) {
+      const int slot = k & 1;
+      if (!__all_sync(0xFFFFFFFFu, wait_unit(k))) { ok = false; break; }
+      const UnitDesc d = udesc[slot];
+      if (!d.valid) break;
+      const int n = (d.n_ent + 1) / 2;
+      // Reference maximum (log2 units) that P, O and the row sums are
+      // relative to.  It moves only when a step's maximum exceeds it by more
+      // than 2^32 (then O is rescaled once); p <= 2^32 keeps every sum far
+      // inside FP32.
+      float ref = -INFINITY;     // reference after the previous step (either group)
+      float my_ref = -INFINITY;  // reference this group's partial sum is kept in
+      float l_run = 0.f;
+      for (int j = ((G & 1) == grp) ? 0 : 1; j < n && ok; j += 2) {
+        const int gs = G + j;
+        const int b = gs % 3;
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_SFULL + b), (gs / 3) & 1, kWaitLimitNs));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t scol = tmem + lane_addr + kColS + 128u * b;
+        // The two 64-key halves come from list entries 2j and 2j+1.  Pass 1
+        // takes the row maximum over both halves, pass 2 reloads each half
+        // from tensor memory and turns it into P (keeps 64 values live).
+        int blk[2], bits[2];
+        entry(d, slot, 2 * j, blk[0], bits[0]);
+        entry(d, slot, 2 * j + 1, blk[1], bits[1]);
+        bool row_ok[2], fast[2], add_bias[2];
+        int nvalid[2];
+        float mx = -INFINITY;
 #pragma unroll
-        for (int q4 = 0; q4 < 16; ++q4) {
-          const float4 bv = add_bias ? __ldg(bb + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
-          const float bq[4] = {bv.x, bv.y, bv.z, bv.w};
+        for (int hh = 0; hh < 2; ++hh) {
+          row_ok[hh] = (bits[hh] >> half) & 1;  // uniform across the warp
+          nvalid[hh] = min(kBlock, g.T - blk[hh] * kBlock);
+          add_bias[hh] = (a.b2 != nullptr) && blk[hh] >= g.nvk;
+          fast[hh] = row_ok[hh] && nvalid[hh] == kBlock && !add_bias[hh];
+          if (!row_ok[hh]) continue;
+          uint32_t sh[64];
+          tmem_ld32(scol + 64u * hh, *reinterpret_cast<uint32_t(*)[32]>(&sh[0]));
+          tmem_ld32(scol + 64u * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&sh[32]));
+          tmem_wait_ld();
+          // Logit in log2 units: l = s * log2(e)/sqrt(128) + b2 (b2 = 0 off
+          // sinks).  Both paths round identically where b2 = 0: the maximum
+          // of fma(s, c, 0) equals c * max(s), and p = 2^fma(s, c, b2 - ref).
+          if (fast[hh]) {
+            mx = fmaxf(mx, max64(sh) * sl2);
+          } else {
+            const float4* bb = reinterpret_cast<const float4*>(a.b2 + static_cast<size_t>(blk[hh]) * kBlock);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int k = 4 * q4 + e;
-            const float bk = (k < nvalid) ? bq[e] : 0.f;
-            const float x = fmaf(__uint_as_float(s[k]), sl2, bk);
-            if (row_ok && k < nvalid) mx = fmaxf(mx, x);
+            for (int q4 = 0; q4 < 16; ++q4) {
+              const float4 bv = add_bias[hh] ? __ldg(bb + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
+              const float bq[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int kx = 4 * q4 + e;
+                const float bk = (kx < nvalid[hh]) ? bq[e] : 0.f;
+                const float x = fmaf(__uint_as_float(sh[kx]), sl2, bk);
+                if (kx < nvalid[hh]) mx = fmaxf(mx, x);
+              }
+            }
           }
         }
-      }
-      const float m_new = fmaxf(m_run, mx);
-      const bool resc = (m_run != -INFINITY) && (m_new > m_run + 8.0f);
-      if (m_run == -INFINITY) m_run = m_new;
-      if (__any_sync(0xFFFFFFFFu, resc)) {
-        // PV_{j-1} must have finished before O is rescaled (j >= 1 here).
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_PVDONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1,
-                                               kWaitLimitNs))) {
-          ok = false;
-          break;
+        // reference after step g-1 of this unit (published by the other group)
+        if (j > 0) {
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_MREADY + (gs - 1) % 3), ((gs - 1) / 3) & 1,
+                                                 kWaitLimitNs))) {
+            ok = false;
+            break;
+          }
+          ref = rref[((gs - 1) % 3) * 128 + row];
         }
-        tc_fence_after();
-        const float alpha = resc ? ex2_approx(m_run - m_new) : 1.0f;
+        const float prev = ref;
+        if (prev == -INFINITY || mx > prev + kRescaleLog2) ref = fmaxf(prev, mx);
+        rref[b * 128 + row] = ref;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_MREADY + b));
+        const bool resc = prev != -INFINITY && ref != prev;
+        if (my_ref != ref) {
+          if (my_ref != -INFINITY) l_run *= ex2_approx(my_ref - ref);
+          my_ref = ref;
+        }
+        const float msub = (ref == -INFINITY) ? 0.f : ref;
+        uint64_t acc[4];
 #pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld32(tmem + lane_addr + kColO + c0, o);
-          tmem_wait_ld();
+        for (int q = 0; q < 4; ++q) acc[q] = f2(0.f, 0.f);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-          tmem_st32(tmem + lane_addr + kColO + c0, o);
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t p[32];
+          if (!row_ok[hh]) {
+#pragma unroll
+            for (int kx = 0; kx < 32; ++kx) p[kx] = 0u;
+          } else {
+            uint32_t sh[64];
+            tmem_ld32(scol + 64u * hh, *reinterpret_cast<uint32_t(*)[32]>(&sh[0]));
+            tmem_ld32(scol + 64u * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&sh[32]));
+            tmem_wait_ld();
+            if (fast[hh]) {
+              // p = 2^(s * scale - ref): one packed FMA per pair, one MUFU per value
+              const uint64_t sc2 = f2(sl2, sl2);
+              const uint64_t nm2 = f2(-msub, -msub);
+#pragma unroll
+              for (int kx = 0; kx < 64; kx += 2) {
+                float x0, x1;
+                unf2(ffma2(f2(__uint_as_float(sh[kx]), __uint_as_float(sh[kx + 1])), sc2, nm2), x0, x1);
+                const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+                acc[(kx >> 1) & 3] = fadd2(acc[(kx >> 1) & 3], f2(e0, e1));
+                p[kx / 2] = pack_bf16x2(e0, e1);
+              }
+            } else {
+              const float4* bb = reinterpret_cast<const float4*>(a.b2 + static_cast<size_t>(blk[hh]) * kBlock);
+#pragma unroll
+              for (int q4 = 0; q4 < 16; ++q4) {
+                const float4 bv = add_bias[hh] ? __ldg(bb + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float bq[4] = {bv.x, bv.y, bv.z, bv.w};
+                float e[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                  const int kx = 4 * q4 + t;
+                  const float bk = (kx < nvalid[hh]) ? bq[t] : 0.f;
+                  const float x = fmaf(__uint_as_float(sh[kx]), sl2, bk - msub);
+                  e[t] = (kx < nvalid[hh]) ? ex2_approx(x) : 0.f;
+                }
+                acc[(2 * q4) & 3] = fadd2(acc[(2 * q4) & 3], f2(e[0], e[1]));
+                acc[(2 * q4 + 1) & 3] = fadd2(acc[(2 * q4 + 1) & 3], f2(e[2], e[3]));
+                p[2 * q4] = pack_bf16x2(e[0], e[1]);
+                p[2 * q4 + 1] = pack_bf16x2(e[2], e[3]);
+              }
+            }
+          }
+          // P (BF16 pairs) of this half into columns [32 hh, 32 hh + 32) of
+          // S_g's buffer: columns already consumed by both passes of half 0.
+          tmem_st32(tmem + lane_addr + kColS + 128u * b + 32u * hh, p);
+        }
+        {
+          float a0, a1, b0, b1, c0, c1, d0, d1;
+          unf2(acc[0], a0, a1);
+          unf2(acc[1], b0, b1);
+          unf2(acc[2], c0, c1);
+          unf2(acc[3], d0, d1);
+          l_run += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
         }
         tmem_wait_st();
-        if (resc) {
-          l_run *= alpha;
-          m_run = m_new;
-        }
-      }
-      const float msub = (m_run == -INFINITY) ? 0.f : m_run;
-      uint32_t p[32];
-      uint64_t acc[4];
-      if (fast) {
-        // p = 2^(s * scale - m): one packed FMA per pair, one MUFU per value
-        const uint64_t sc2 = f2(sl2, sl2);
-        const uint64_t nm2 = f2(-msub, -msub);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[q] = f2(0.f, 0.f);
-#pragma unroll
-        for (int k = 0; k < 64; k += 2) {
-          float x0, x1;
-          unf2(ffma2(f2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), sc2, nm2), x0, x1);
-          const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
-          acc[(k >> 1) & 3] = fadd2(acc[(k >> 1) & 3], f2(e0, e1));
-          p[k / 2] = pack_bf16x2(e0, e1);
-        }
-      } else {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[q] = f2(0.f, 0.f);
-        float e[64];
-#pragma unroll
-        for (int q4 = 0; q4 < 16; ++q4) {
-          const float4 bv = add_bias ? __ldg(bb + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
-          const float bq[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int k = 4 * q4 + t;
-            const float bk = (k < nvalid) ? bq[t] : 0.f;
-            const float x = fmaf(__uint_as_float(s[k]), sl2, bk - msub);
-            e[k] = (row_ok && k < nvalid) ? ex2_approx(x) : 0.f;
+        // O holds sum_{i<g} P_i V_i relative to `prev`; move it to `ref`
+        // before P_g is released to the MMA thread.
+        if (__any_sync(0xFFFFFFFFu, resc)) {
+          // PV_{g-1} must have finished before O is rescaled (j >= 1 here).
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_PVDONE + (gs - 1) % 3), ((gs - 1) / 3) & 1,
+                                                 kWaitLimitNs))) {
+            ok = false;
+            break;
           }
-        }
+          tc_fence_after();
+          const float alpha = resc ? ex2_approx(prev - ref) : 1.0f;
 #pragma unroll
-        for (int k = 0; k < 64; k += 2) {
-          acc[(k >> 1) & 3] = fadd2(acc[(k >> 1) & 3], f2(e[k], e[k + 1]));
-          p[k / 2] = pack_bf16x2(e[k], e[k + 1]);
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_addr + kColO + c0, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st32(tmem + lane_addr + kColO + c0, o);
+          }
+          tmem_wait_st();
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_PFULL + b));
+        if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) ok = false;
       }
-      {
-        float a0, a1, b0, b1, c0, c1, d0, d1;
-        unf2(acc[0], a0, a1);
-        unf2(acc[1], b0, b1);
-        unf2(acc[2], c0, c1);
-        unf2(acc[3], d0, d1);
-        l_run += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+      // ---- epilogue of the unit
+      ok = ok && __all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_OFULL), k & 1, kWaitLimitNs));
+      const int last = G + n - 1;
+      if (ok && (last & 1) != grp)  // the other group published the last reference
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_MREADY + last % 3), (last / 3) & 1, kWaitLimitNs));
+      float fin = -INFINITY;
+      if (ok) {
+        tc_fence_after();
+        fin = rref[(last % 3) * 128 + row];
       }
-      tmem_st32(tmem + lane_addr + kColS + 64u * b, p);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_PFULL + b));
-      if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) { ok = false; break; }
-    }
-    if (ok && !__all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_OFULL), 0, kWaitLimitNs))) ok = false;
-    if (!ok) {
-      *s_abort = 1;
-      set_status(a.status, 5 /* SA_ETIMEOUT */);
-    } else {
-      tc_fence_after();
-      // ---- epilogue: O / l -> BF16
+      const float l_mine = (my_ref == -INFINITY || !ok) ? 0.f : l_run * ex2_approx(my_ref - fin);
+      xl[grp * 128 + row] = l_mine;
+      // both groups meet here; the OR-reduction makes the outcome uniform
+      ok = !named_bar_or(2, kSoftmaxThreads, !ok || *s_abort != 0);
+      const float l_tot = l_mine + xl[(grp ^ 1) * 128 + row];
+      if (!ok) break;
       int t;
       bool real;
-      if (dense) {
-        t = row0 + row;
+      if (d.dense) {
+        t = d.row0 + row;
         real = t < g.T;
       } else {
-        const int ib = half ? iB : iA;
+        const int ib = half ? d.iB : d.iA;
         const int r = row & 63;
         t = kBlock * ib + r;
         const int nreal = (ib < 0) ? 0 : (ib < g.nvk ? kBlock : g.tail);
         real = ib >= 0 && r < nreal;
       }
-      const float inv_l = (l_run > 0.f) ? 1.0f / l_run : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(a.o + (static_cast<size_t>(t) * g.H + h) * kHeadDim);
+      const float inv_l = (l_tot > 0.f) ? 1.0f / l_tot : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(a.o + (static_cast<size_t>(t) * g.H + d.h) * kHeadDim + 64 * grp);
 #pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
+      for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_addr + kColO + c0, o);
+        tmem_ld32(tmem + lane_addr + kColO + 64u * grp + c0, o);
         tmem_wait_ld();
         if (real) {
 #pragma unroll
@@ -533,6 +741,21 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           }
         }
       }
+      // O has been read: the next unit's first PV may overwrite it.  The
+      // second named barrier keeps the exchanged sums stable until both
+      // groups have read them.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(BAR_OEMPTY));
+        mbar_arrive(bar(BAR_UEMPTY + slot));
+      }
+      ok = !named_bar_or(2, kSoftmaxThreads, *s_abort != 0);
+      G += n;
+    }
+    if (!ok) {
+      *s_abort = 1;
+      set_status(a.status, 5 /* SA_ETIMEOUT */);
     }
   }
 
@@ -557,6 +780,18 @@ __global__ void bias_prep_kernel(const float* __restrict__ bias, float* __restri
   }
 }
 
+int sm_count() {
+  static int cached[128] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 }  // namespace
 
 size_t attention_smem_bytes() { return kSmemBytes; }
@@ -577,7 +812,8 @@ cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const
   if (e != cudaSuccess) return e;
   const int units = a.g.H * (a.n_dense + a.n_pairs);
   if (units == 0) return cudaSuccess;
-  attention_kernel<<<units, kThreads, kSmemBytes, s>>>(tq, tk, tv, a);
+  const int grid = units < sm_count() ? units : sm_count();
+  attention_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
 

@@ -46,6 +46,7 @@ struct AttnArgs {
   const float* b2;     // key bias in log2 units [T], or null
   uint16_t* o;         // BF16 bits [T, H, 128]
   int32_t* status;     // device status word
+  int32_t* unit_counter;  // next work unit (zeroed before the launch)
   Geometry g;
   int n_dense;         // dense 128-row tiles per head
   int n_pairs;         // sparse query-block pairs per head

@@ -28,8 +28,8 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // 16-byte slices, so every row is read with full coalescing.  HBM-bound.
 constexpr int kPoolThreads = 256;
 
-__global__ void __launch_bounds__(kPoolThreads) pool_kernel(PlanArgs a, int nchunks) {
-  const Geometry& g = a.g;
+__global__ void __launch_bounds__(kPoolThreads) pool_kernel(const PlanArgs a, int nchunks) {
+  const Geometry g = a.g;
   const bool isq = blockIdx.y == 0;
   const int nblocks = isq ? g.nq : g.nvk;
   const int i = blockIdx.x / nchunks;
@@ -68,19 +68,28 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 constexpr int kRouteThreads = 256;
-constexpr int kKeyChunk = 64;        // Kmean rows staged per step
+constexpr int kKeyChunk = 128;           // Kmean rows staged per step
 constexpr int kKcStride = kHeadDim + 1;  // padded row: conflict-free column reads
 
-// One CTA per (QB query blocks, head).  Phase 1: the QB x nvk score strip in
-// shared memory, FP32 FMA over d = 0..127 in order.  Phase 2: one warp per
-// query block runs the radix search for the K'-th largest key and emits the
-// sorted union of forced local blocks, selected blocks and sinks.
-template <int QB>
+// One CTA per (QB query blocks, head).
+// Phase 1: the QB x nvk score strip in shared memory.  Each thread owns QPT
+// query blocks x KPT key blocks of every 128-key chunk and accumulates
+// s = sum_d Qmean[d] Kmean[d] in FP32, d = 0..127 in order; the query values
+// are broadcast reads, the key values come from padded rows (consecutive
+// lanes take consecutive keys, so the reads are conflict-free).
+// Phase 2: one warp per query block turns its scores into order-preserving
+// keys (forced local blocks become key 0, below every score), runs the radix
+// search for the K'-th largest key and emits the sorted union of forced local
+// blocks, selected blocks and sinks.
+template <int QB, int QPT, int KPT>
 __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
+  constexpr int NQG = QB / QPT;              // query groups
+  constexpr int NKG = kRouteThreads / NQG;   // key groups
+  static_assert(NKG * KPT == kKeyChunk, "chunk mapping");
   const Geometry& g = a.g;
   extern __shared__ __align__(16) float rsm[];
   float* qcT = rsm;                              // [128][QB]
-  float* kcs = qcT + kHeadDim * QB;              // [64][129]
+  float* kcs = qcT + kHeadDim * QB;              // [128][129]
   float* sc = kcs + kKeyChunk * kKcStride;       // [QB][nvk]
   const int h = blockIdx.y;
   const int i0 = blockIdx.x * QB;
@@ -92,9 +101,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
     qcT[d * QB + qi] = (i < g.nq) ? a.qc[(static_cast<size_t>(h) * g.nq + i) * kHeadDim + d] : 0.f;
   }
 
-  constexpr int QPT = QB / 4;  // query blocks per thread
-  const int jl = tid % kKeyChunk;
-  const int grp = tid / kKeyChunk;
+  const int kg = tid % NKG;
+  const int qg = tid / NKG;
   const float inv_sqrt_d = 0.08838834764831845f;  // 1/sqrt(128)
   for (int j0 = 0; j0 < g.nvk; j0 += kKeyChunk) {
     __syncthreads();
@@ -108,21 +116,29 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
       dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
     }
     __syncthreads();
-    float acc[QPT];
+    float acc[QPT][KPT];
 #pragma unroll
-    for (int e = 0; e < QPT; ++e) acc[e] = 0.f;
-    const float* krow = kcs + jl * kKcStride;
+    for (int q = 0; q < QPT; ++q)
+#pragma unroll
+      for (int e = 0; e < KPT; ++e) acc[q][e] = 0.f;
 #pragma unroll 4
     for (int d = 0; d < kHeadDim; ++d) {
-      const float kv = krow[d];
-      const float* qv = qcT + d * QB + grp * QPT;
+      float kv[KPT];
 #pragma unroll
-      for (int e = 0; e < QPT; ++e) acc[e] = fmaf(qv[e], kv, acc[e]);
+      for (int e = 0; e < KPT; ++e) kv[e] = kcs[(kg + NKG * e) * kKcStride + d];
+      const float* qv = qcT + d * QB + qg * QPT;
+#pragma unroll
+      for (int q = 0; q < QPT; ++q)
+#pragma unroll
+        for (int e = 0; e < KPT; ++e) acc[q][e] = fmaf(qv[q], kv[e], acc[q][e]);
     }
-    const int j = j0 + jl;
-    if (j < g.nvk) {
 #pragma unroll
-      for (int e = 0; e < QPT; ++e) sc[(grp * QPT + e) * g.nvk + j] = acc[e] * inv_sqrt_d;
+    for (int e = 0; e < KPT; ++e) {
+      const int j = j0 + kg + NKG * e;
+      if (j < g.nvk) {
+#pragma unroll
+        for (int q = 0; q < QPT; ++q) sc[(qg * QPT + q) * g.nvk + j] = acc[q][e] * inv_sqrt_d;
+      }
     }
   }
   __syncthreads();
@@ -134,6 +150,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
       float* dst = a.scores + (static_cast<size_t>(h) * g.nq + i) * g.nvk;
       for (int j = tid; j < g.nvk; j += kRouteThreads) dst[j] = sc[qi * g.nvk + j];
     }
+    __syncthreads();
   }
 
   const int warp = tid / 32, lane = tid % 32;
@@ -141,28 +158,31 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
   for (int qi = warp; qi < QB; qi += kRouteThreads / 32) {
     const int i = i0 + qi;
     if (i >= g.nq) break;
-    const float* srow = sc + qi * g.nvk;
+    uint32_t* krow = reinterpret_cast<uint32_t*>(sc + qi * g.nvk);
     const int lo = max(0, i - g.R);
     const int hi = min(g.nvk - 1, i + g.R);
     const int nlv = max(0, hi - lo + 1);
     const int ncand = g.nvk - nlv;
     const int kp = min(g.K, ncand);
     const bool take_all = (kp == ncand);
+    for (int j = lane; j < g.nvk; j += 32) {
+      const float f = __uint_as_float(krow[j]);
+      krow[j] = (j >= lo && j <= hi) ? 0u : order_key(f);
+    }
+    __syncwarp();
     uint32_t tau = 0;
     int need = 0;
     if (!take_all) {
-      // Largest tau with #{candidates with key >= tau} >= kp, bit by bit.
+      // Largest tau with #{candidate keys >= tau} >= kp, bit by bit.
       for (int bit = 31; bit >= 0; --bit) {
         const uint32_t t = tau | (1u << bit);
         int c = 0;
-        for (int j = lane; j < g.nvk; j += 32)
-          c += ((j < lo || j > hi) && order_key(srow[j]) >= t) ? 1 : 0;
+        for (int j = lane; j < g.nvk; j += 32) c += (krow[j] >= t) ? 1 : 0;
         c = __reduce_add_sync(0xFFFFFFFFu, c);
         if (c >= kp) tau = t;
       }
       int gt = 0;
-      for (int j = lane; j < g.nvk; j += 32)
-        gt += ((j < lo || j > hi) && order_key(srow[j]) > tau) ? 1 : 0;
+      for (int j = lane; j < g.nvk; j += 32) gt += (krow[j] > tau) ? 1 : 0;
       gt = __reduce_add_sync(0xFFFFFFFFu, gt);
       need = kp - gt;
     }
@@ -177,7 +197,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
         } else if (take_all) {
           sel = true;
         } else {
-          const uint32_t kk = order_key(srow[j]);
+          const uint32_t kk = krow[j];
           if (kk > tau) sel = true;
           else if (kk == tau) eq = true;
         }
@@ -197,8 +217,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
 }
 
 int route_qb(const Geometry& g) {
-  if (g.nvk <= 1536) return 16;
-  if (g.nvk <= 3072) return 8;
+  if (g.nvk <= 1024) return 32;
+  if (g.nvk <= 2048) return 16;
+  if (g.nvk <= 4096) return 8;
   return 4;
 }
 
@@ -218,27 +239,24 @@ cudaError_t launch_pool(const PlanArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_route_topk(const PlanArgs& a, cudaStream_t s) {
-  const int qb = route_qb(a.g);
-  const size_t smem = route_topk_smem_bytes(a.g);
-  const dim3 grid((a.g.nq + qb - 1) / qb, a.g.H);
-  cudaError_t e = cudaSuccess;
-  switch (qb) {
-    case 16:
-      e = cudaFuncSetAttribute(route_topk_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) route_topk_kernel<16><<<grid, kRouteThreads, smem, s>>>(a);
-      break;
-    case 8:
-      e = cudaFuncSetAttribute(route_topk_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) route_topk_kernel<8><<<grid, kRouteThreads, smem, s>>>(a);
-      break;
-    default:
-      e = cudaFuncSetAttribute(route_topk_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) route_topk_kernel<4><<<grid, kRouteThreads, smem, s>>>(a);
-      break;
-  }
+template <int QB, int QPT, int KPT>
+static cudaError_t launch_route_variant(const PlanArgs& a, size_t smem, cudaStream_t s) {
+  auto* k = route_topk_kernel<QB, QPT, KPT>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  const dim3 grid((a.g.nq + QB - 1) / QB, a.g.H);
+  k<<<grid, kRouteThreads, smem, s>>>(a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_route_topk(const PlanArgs& a, cudaStream_t s) {
+  const size_t smem = route_topk_smem_bytes(a.g);
+  switch (route_qb(a.g)) {
+    case 32: return launch_route_variant<32, 4, 4>(a, smem, s);
+    case 16: return launch_route_variant<16, 4, 2>(a, smem, s);
+    case 8: return launch_route_variant<8, 4, 1>(a, smem, s);
+    default: return launch_route_variant<4, 2, 1>(a, smem, s);
+  }
 }
 
 }  // namespace sa

@@ -175,6 +175,13 @@ sa_status sparse_attn_plan_static(const sa_params* p, const void* q, const void*
  */
 sa_status sparse_attn_last_device_status(const void* ws, cudaStream_t stream, sa_status* out);
 
+/*
+ * The last CUDA runtime error that made an entry point return SA_ECUDA on
+ * the calling host thread (0 = none since the thread started), and its
+ * message when `message` is not NULL.  Host only.
+ */
+int sparse_attn_last_cuda_error(const char** message);
+
 /* Static, human-readable name of a status code. */
 const char* sparse_attn_status_string(sa_status s);
 
