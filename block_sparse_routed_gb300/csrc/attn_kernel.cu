@@ -37,15 +37,17 @@
 // complete; two K-steps of PV_g are issued before that wait to keep the pipe
 // busy.
 //
-// Warp roles (11 warps): warp 0 issues TMA loads (Q per unit; K and V per
-// step through a 4-slot ring), warp 1 owns tensor memory and issues the MMAs
-// (one thread), warps 2-5 (softmax group 0) and 6-9 (group 1) each own one
-// query row per thread (= tensor-memory lane); group 0 takes even global
-// steps and group 1 odd ones, all 128 columns each, so two steps' softmax run
-// at once.  The groups share one lazily updated reference maximum per row,
-// passed step to step through shared memory; each keeps a partial row sum;
-// both merge and store the output in the unit's epilogue.  Warp 10 schedules
-// units and merges their block lists.
+// Warp roles (12 warps, three warpgroups): warpgroup 0 holds the
+// single-thread roles: warp 0 issues TMA loads (Q per unit; K and V per step
+// through a 4-slot ring), warp 1 owns tensor memory and issues the MMAs (one
+// thread), warp 2 schedules units and merges their block lists, warp 3 idles.
+// Warpgroups 1 (warps 4-7, softmax group 0) and 2 (warps 8-11, group 1) each
+// own one query row per thread (= tensor-memory lane); group 0 takes even
+// global steps and group 1 odd ones, all 128 columns each, so two steps'
+// softmax run at once.  The groups share one lazily updated reference maximum
+// per row, passed step to step through shared memory; each keeps a partial
+// row sum; both merge and store the output in the unit's epilogue.
+// Warpgroup 0 hands registers to the softmax warpgroups (setmaxnreg).
 //
 // Tensor memory (512 columns): O in [0, 128); S buffers at 128, 256, 384.
 #include <cstdint>
@@ -56,8 +58,14 @@
 namespace sa {
 namespace {
 
-constexpr int kThreads = 352;
-constexpr int kSoftmaxThreads = 256;  // warps 2..9
+constexpr int kThreads = 384;
+constexpr int kSoftmaxThreads = 256;  // warps 4..11
+// Register budgets after the split: warpgroup 0 (single-thread roles) gives
+// registers to the two softmax warpgroups.  128 x 88 + 256 x 208 = 64512 =
+// 384 x 168, the block's allocation at launch.
+constexpr uint32_t kRegsControl = 88;
+constexpr uint32_t kRegsSoftmax = 208;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "register split");
 constexpr int kTmemCols = 512;
 constexpr uint32_t kColO = 0;
 constexpr uint32_t kColS = 128;  // S buffer b at kColS + 128 b, b in {0, 1, 2}
@@ -277,7 +285,10 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     return mbar_wait(bar(BAR_UFULL + (k & 1)), (k >> 1) & 1, kWaitLimitNs);
   };
 
-  if (warp == 10) {
+  if (warp < 4) {
+    setmaxnreg_dec<kRegsControl>();
+  }
+  if (warp == 2) {
     // ------------------------------------------------------------ scheduler
     int32_t* la = reinterpret_cast<int32_t*>(base + kOffScratch);
     int32_t* lb = la + kMaxList;
@@ -333,12 +344,12 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
               const int m = m0 + lane;
               int32_t cur = 0, nxt = -1;
               if (m < nm) cur = mg[m];
-              if (m + 1 < nm) nxt = mg[m + 1] & kEntBlockMask;
-              const int32_t blk = (m < nm) ? (cur & kEntBlockMask) : -2;
+              if (m + 1 < nm) nxt = static_cast<int32_t>(static_cast<uint32_t>(mg[m + 1]) & kEntBlockMask);
+              const int32_t blk = (m < nm) ? static_cast<int32_t>(static_cast<uint32_t>(cur) & kEntBlockMask) : -2;
               int32_t before = __shfl_up_sync(0xFFFFFFFFu, blk, 1);
               if (lane == 0) before = prev_blk;
               const bool keep = m < nm && blk != before;
-              const int32_t val = (nxt == blk) ? static_cast<int32_t>(blk | (3u << kEntMaskShift)) : cur;
+              const int32_t val = (nxt == blk) ? static_cast<int32_t>(static_cast<uint32_t>(blk) | (3u << kEntMaskShift)) : cur;
               prev_blk = __shfl_sync(0xFFFFFFFFu, blk, 31);
               const unsigned km = __ballot_sync(0xFFFFFFFFu, keep);
               __syncwarp();  // all reads of this chunk precede its writes
@@ -514,9 +525,10 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         mbar_wait(bar(BAR_DRAIN), 0, kWaitLimitNs);
       }
     }
-  } else {
+  } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
-    const int grp = (warp - 2) / 4;        // owns global steps with parity grp
+    setmaxnreg_inc<kRegsSoftmax>();
+    const int grp = (warp - 4) / 4;        // owns global steps with parity grp
     const int quad = warp & 3;             // tensor-memory lane quarter of this warp
     const int row = quad * 32 + lane;      // query row within the tile
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
@@ -810,6 +822,17 @@ cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const
   cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
+  // The register split redistributes the block's launch allocation; a build
+  // that allocated fewer registers per thread would make setmaxnreg.inc wait
+  // forever, so refuse to launch it.
+  static int regs = -1;
+  if (regs < 0) {
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, attention_kernel);
+    if (e != cudaSuccess) return e;
+    regs = fa.numRegs;
+  }
+  if (regs * kThreads < static_cast<int>(128 * kRegsControl + 256 * kRegsSoftmax)) return cudaErrorInvalidConfiguration;
   const int units = a.g.H * (a.n_dense + a.n_pairs);
   if (units == 0) return cudaSuccess;
   const int grid = units < sm_count() ? units : sm_count();

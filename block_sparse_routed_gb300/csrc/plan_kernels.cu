@@ -78,9 +78,10 @@ constexpr int kKcStride = kHeadDim + 1;  // padded row: conflict-free column rea
 // are broadcast reads, the key values come from padded rows (consecutive
 // lanes take consecutive keys, so the reads are conflict-free).
 // Phase 2: one warp per query block turns its scores into order-preserving
-// keys (forced local blocks become key 0, below every score), runs the radix
-// search for the K'-th largest key and emits the sorted union of forced local
-// blocks, selected blocks and sinks.
+// keys (forced local blocks become key 0, below every score), finds the
+// K'-th largest key exactly by a most-significant-digit-first radix select
+// (four 8-bit digits, a 256-bin histogram per pass) and emits the sorted
+// union of forced local blocks, selected blocks and sinks.
 template <int QB, int QPT, int KPT>
 __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
   constexpr int NQG = QB / QPT;              // query groups
@@ -91,6 +92,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
   float* qcT = rsm;                              // [128][QB]
   float* kcs = qcT + kHeadDim * QB;              // [128][129]
   float* sc = kcs + kKeyChunk * kKcStride;       // [QB][nvk]
+  int* hist_all = reinterpret_cast<int*>(sc + QB * g.nvk);  // [warps][256]
   const int h = blockIdx.y;
   const int i0 = blockIdx.x * QB;
   const int tid = threadIdx.x;
@@ -126,7 +128,19 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
       float kv[KPT];
 #pragma unroll
       for (int e = 0; e < KPT; ++e) kv[e] = kcs[(kg + NKG * e) * kKcStride + d];
-      const float* qv = qcT + d * QB + qg * QPT;
+      // the QPT query values are contiguous and 8/16-byte aligned: vector loads
+      float qv[QPT];
+      if constexpr (QPT % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < QPT; q += 4) {
+          const float4 t = *reinterpret_cast<const float4*>(qcT + d * QB + qg * QPT + q);
+          qv[q] = t.x; qv[q + 1] = t.y; qv[q + 2] = t.z; qv[q + 3] = t.w;
+        }
+      } else {
+        static_assert(QPT == 2, "query values per thread");
+        const float2 t = *reinterpret_cast<const float2*>(qcT + d * QB + qg * QPT);
+        qv[0] = t.x; qv[1] = t.y;
+      }
 #pragma unroll
       for (int q = 0; q < QPT; ++q)
 #pragma unroll
@@ -173,18 +187,57 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
     uint32_t tau = 0;
     int need = 0;
     if (!take_all) {
-      // Largest tau with #{candidate keys >= tau} >= kp, bit by bit.
-      for (int bit = 31; bit >= 0; --bit) {
-        const uint32_t t = tau | (1u << bit);
-        int c = 0;
-        for (int j = lane; j < g.nvk; j += 32) c += (krow[j] >= t) ? 1 : 0;
-        c = __reduce_add_sync(0xFFFFFFFFu, c);
-        if (c >= kp) tau = t;
+      // Digits of the kp-th largest key, most significant first.  `need`
+      // counts how many keys equal to the prefix found so far still have to
+      // be taken; the keys above the prefix's bin are already counted out.
+      int* hist = hist_all + warp * 256;
+      uint32_t prefix = 0, pmask = 0;
+      need = kp;
+#pragma unroll 1
+      for (int shift = 24; shift >= 0; shift -= 8) {
+#pragma unroll
+        for (int b = 0; b < 8; ++b) hist[lane * 8 + b] = 0;
+        __syncwarp();
+        for (int j = lane; j < g.nvk; j += 32) {
+          const uint32_t kk = krow[j];
+          if ((kk & pmask) == prefix) atomicAdd(&hist[(kk >> shift) & 255u], 1);
+        }
+        __syncwarp();
+        // lane l owns bins 8l..8l+7; count from the top bin down
+        int c[8], tot = 0;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) { c[b] = hist[lane * 8 + b]; tot += c[b]; }
+        int above = tot;  // keys in this lane's bins and every higher lane's
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_down_sync(0xFFFFFFFFu, above, o);
+          if (lane + o < 32) above += v;
+        }
+        const int higher = above - tot;  // keys in higher lanes' bins
+        // the digit's lane: higher < need <= above
+        const unsigned own = __ballot_sync(0xFFFFFFFFu, higher < need && need <= above);
+        const int src = __ffs(own) - 1;
+        int digit = 0, rem = 0;
+        if (lane == src) {
+          int acc = higher;
+          bool found = false;
+#pragma unroll
+          for (int b = 7; b >= 0; --b) {
+            if (!found && acc + c[b] >= need) {
+              found = true;
+              digit = lane * 8 + b;
+              rem = need - acc;
+            }
+            acc += c[b];
+          }
+        }
+        digit = __shfl_sync(0xFFFFFFFFu, digit, src);
+        need = __shfl_sync(0xFFFFFFFFu, rem, src);
+        prefix |= static_cast<uint32_t>(digit) << shift;
+        pmask |= 255u << shift;
+        __syncwarp();
       }
-      int gt = 0;
-      for (int j = lane; j < g.nvk; j += 32) gt += (krow[j] > tau) ? 1 : 0;
-      gt = __reduce_add_sync(0xFFFFFFFFu, gt);
-      need = kp - gt;
+      tau = prefix;
     }
     int32_t* out = a.idx + (static_cast<size_t>(h) * g.nq + i) * g.maxl;
     int pos = 0, eq_seen = 0;
@@ -228,7 +281,7 @@ int route_qb(const Geometry& g) {
 size_t route_topk_smem_bytes(const Geometry& g) {
   const int qb = route_qb(g);
   return sizeof(float) * (static_cast<size_t>(kHeadDim) * qb + kKeyChunk * kKcStride +
-                          static_cast<size_t>(qb) * g.nvk);
+                          static_cast<size_t>(qb) * g.nvk + (kRouteThreads / 32) * 256);
 }
 
 cudaError_t launch_pool(const PlanArgs& a, cudaStream_t s) {
@@ -252,7 +305,7 @@ static cudaError_t launch_route_variant(const PlanArgs& a, size_t smem, cudaStre
 cudaError_t launch_route_topk(const PlanArgs& a, cudaStream_t s) {
   const size_t smem = route_topk_smem_bytes(a.g);
   switch (route_qb(a.g)) {
-    case 32: return launch_route_variant<32, 4, 4>(a, smem, s);
+    case 32: return launch_route_variant<32, 8, 2>(a, smem, s);
     case 16: return launch_route_variant<16, 4, 2>(a, smem, s);
     case 8: return launch_route_variant<8, 4, 1>(a, smem, s);
     default: return launch_route_variant<4, 2, 1>(a, smem, s);
