@@ -79,10 +79,11 @@ constexpr int kKcStride = kHeadDim + 1;  // padded row: conflict-free column rea
 // lanes take consecutive keys, so the reads are conflict-free).
 // Phase 2: one warp per query block turns its scores into order-preserving
 // keys (forced local blocks become key 0, below every score), finds the
-// K'-th largest key exactly by a most-significant-digit-first radix select
-// (four 8-bit digits, a 256-bin histogram per pass) and emits the sorted
-// union of forced local blocks, selected blocks and sinks.
-template <int QB, int QPT, int KPT>
+// K'-th largest key exactly by a bitwise radix search (keys held in
+// registers, KPL per lane, when the row fits; else read from shared memory)
+// and emits the sorted union of forced local blocks, selected blocks and
+// sinks.
+template <int QB, int QPT, int KPT, int KPL>
 __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
   constexpr int NQG = QB / QPT;              // query groups
   constexpr int NKG = kRouteThreads / NQG;   // key groups
@@ -92,15 +93,36 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
   float* qcT = rsm;                              // [128][QB]
   float* kcs = qcT + kHeadDim * QB;              // [128][129]
   float* sc = kcs + kKeyChunk * kKcStride;       // [QB][nvk]
-  int* hist_all = reinterpret_cast<int*>(sc + QB * g.nvk);  // [warps][256]
   const int h = blockIdx.y;
   const int i0 = blockIdx.x * QB;
   const int tid = threadIdx.x;
 
-  for (int e = tid; e < QB * kHeadDim; e += kRouteThreads) {
-    const int qi = e / kHeadDim, d = e % kHeadDim;
-    const int i = i0 + qi;
-    qcT[d * QB + qi] = (i < g.nq) ? a.qc[(static_cast<size_t>(h) * g.nq + i) * kHeadDim + d] : 0.f;
+  // Qmean strip, transposed: consecutive lanes take consecutive query blocks
+  // (conflict-free stores); all of a thread's loads are issued before its
+  // stores.
+  {
+    constexpr int kTot = QB * (kHeadDim / 4);
+    constexpr int kPer = (kTot + kRouteThreads - 1) / kRouteThreads;
+    float4 v[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int e = tid + u * kRouteThreads;
+      const int qi = e % QB, d4 = e / QB;
+      const int i = i0 + qi;
+      v[u] = (e < kTot && i < g.nq)
+                 ? *reinterpret_cast<const float4*>(a.qc + (static_cast<size_t>(h) * g.nq + i) * kHeadDim + 4 * d4)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int e = tid + u * kRouteThreads;
+      if (e >= kTot) break;
+      const int qi = e % QB, d4 = e / QB;
+      qcT[(4 * d4 + 0) * QB + qi] = v[u].x;
+      qcT[(4 * d4 + 1) * QB + qi] = v[u].y;
+      qcT[(4 * d4 + 2) * QB + qi] = v[u].z;
+      qcT[(4 * d4 + 3) * QB + qi] = v[u].w;
+    }
   }
 
   const int kg = tid % NKG;
@@ -108,22 +130,35 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
   const float inv_sqrt_d = 0.08838834764831845f;  // 1/sqrt(128)
   for (int j0 = 0; j0 < g.nvk; j0 += kKeyChunk) {
     __syncthreads();
-    for (int e = tid; e < kKeyChunk * (kHeadDim / 4); e += kRouteThreads) {
-      const int r = e / (kHeadDim / 4), c4 = e % (kHeadDim / 4);
-      const int j = j0 + r;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (j < g.nvk)
-        v = *reinterpret_cast<const float4*>(a.kc + (static_cast<size_t>(h) * g.nvk + j) * kHeadDim + 4 * c4);
-      float* dst = kcs + r * kKcStride + 4 * c4;
-      dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
+    // Kmean chunk: loads in batches of 8 per thread, then the stores.
+    constexpr int kPerK = kKeyChunk * (kHeadDim / 4) / kRouteThreads;
+    static_assert(kPerK % 8 == 0, "Kmean fill mapping");
+#pragma unroll 1
+    for (int u0 = 0; u0 < kPerK; u0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int e = tid + (u0 + u) * kRouteThreads;
+        const int j = j0 + e / (kHeadDim / 4), c4 = e % (kHeadDim / 4);
+        v[u] = (j < g.nvk) ? *reinterpret_cast<const float4*>(a.kc + (static_cast<size_t>(h) * g.nvk + j) * kHeadDim + 4 * c4)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int e = tid + (u0 + u) * kRouteThreads;
+        float* dst = kcs + (e / (kHeadDim / 4)) * kKcStride + 4 * (e % (kHeadDim / 4));
+        dst[0] = v[u].x; dst[1] = v[u].y; dst[2] = v[u].z; dst[3] = v[u].w;
+      }
     }
     __syncthreads();
+    // a thread whose first key is past the end has no key in this chunk
+    if (j0 + kg >= g.nvk) continue;
     float acc[QPT][KPT];
 #pragma unroll
     for (int q = 0; q < QPT; ++q)
 #pragma unroll
       for (int e = 0; e < KPT; ++e) acc[q][e] = 0.f;
-#pragma unroll 4
+#pragma unroll 8
     for (int d = 0; d < kHeadDim; ++d) {
       float kv[KPT];
 #pragma unroll
@@ -169,88 +204,35 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
 
   const int warp = tid / 32, lane = tid % 32;
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int qi = warp; qi < QB; qi += kRouteThreads / 32) {
-    const int i = i0 + qi;
-    if (i >= g.nq) break;
-    uint32_t* krow = reinterpret_cast<uint32_t*>(sc + qi * g.nvk);
-    const int lo = max(0, i - g.R);
-    const int hi = min(g.nvk - 1, i + g.R);
-    const int nlv = max(0, hi - lo + 1);
-    const int ncand = g.nvk - nlv;
-    const int kp = min(g.K, ncand);
-    const bool take_all = (kp == ncand);
-    for (int j = lane; j < g.nvk; j += 32) {
-      const float f = __uint_as_float(krow[j]);
-      krow[j] = (j >= lo && j <= hi) ? 0u : order_key(f);
-    }
-    __syncwarp();
-    uint32_t tau = 0;
-    int need = 0;
-    if (!take_all) {
-      // Digits of the kp-th largest key, most significant first.  `need`
-      // counts how many keys equal to the prefix found so far still have to
-      // be taken; the keys above the prefix's bin are already counted out.
-      int* hist = hist_all + warp * 256;
-      uint32_t prefix = 0, pmask = 0;
-      need = kp;
-#pragma unroll 1
-      for (int shift = 24; shift >= 0; shift -= 8) {
-#pragma unroll
-        for (int b = 0; b < 8; ++b) hist[lane * 8 + b] = 0;
-        __syncwarp();
-        for (int j = lane; j < g.nvk; j += 32) {
-          const uint32_t kk = krow[j];
-          if ((kk & pmask) == prefix) atomicAdd(&hist[(kk >> shift) & 255u], 1);
-        }
-        __syncwarp();
-        // lane l owns bins 8l..8l+7; count from the top bin down
-        int c[8], tot = 0;
-#pragma unroll
-        for (int b = 0; b < 8; ++b) { c[b] = hist[lane * 8 + b]; tot += c[b]; }
-        int above = tot;  // keys in this lane's bins and every higher lane's
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int v = __shfl_down_sync(0xFFFFFFFFu, above, o);
-          if (lane + o < 32) above += v;
-        }
-        const int higher = above - tot;  // keys in higher lanes' bins
-        // the digit's lane: higher < need <= above
-        const unsigned own = __ballot_sync(0xFFFFFFFFu, higher < need && need <= above);
-        const int src = __ffs(own) - 1;
-        int digit = 0, rem = 0;
-        if (lane == src) {
-          int acc = higher;
-          bool found = false;
-#pragma unroll
-          for (int b = 7; b >= 0; --b) {
-            if (!found && acc + c[b] >= need) {
-              found = true;
-              digit = lane * 8 + b;
-              rem = need - acc;
-            }
-            acc += c[b];
-          }
-        }
-        digit = __shfl_sync(0xFFFFFFFFu, digit, src);
-        need = __shfl_sync(0xFFFFFFFFu, rem, src);
-        prefix |= static_cast<uint32_t>(digit) << shift;
-        pmask |= 255u << shift;
-        __syncwarp();
-      }
-      tau = prefix;
-    }
-    int32_t* out = a.idx + (static_cast<size_t>(h) * g.nq + i) * g.maxl;
+  // Per query block i: forced local range [lo, hi], budget kp.
+  struct Row {
+    int i, lo, hi, kp;
+    bool take_all;
+  };
+  auto row_of = [&](int qi) {
+    Row r;
+    r.i = i0 + qi;
+    r.lo = max(0, r.i - g.R);
+    r.hi = min(g.nvk - 1, r.i + g.R);
+    const int ncand = g.nvk - max(0, r.hi - r.lo + 1);
+    r.kp = min(g.K, ncand);
+    r.take_all = (r.kp == ncand);
+    return r;
+  };
+  // Writes row r's sorted list: `key_of(j)` gives block j's key (j < nvk).
+  // Keys above tau are taken, keys equal to tau lowest index first until
+  // `need` of them are, forced local blocks and sinks always.
+  auto emit_row = [&](const Row& r, uint32_t tau, int need, auto key_of) {
+    int32_t* out = a.idx + (static_cast<size_t>(h) * g.nq + r.i) * g.maxl;
     int pos = 0, eq_seen = 0;
     for (int j0 = 0; j0 < g.nblk; j0 += 32) {
       const int j = j0 + lane;
       bool sel = false, eq = false;
       if (j < g.nvk) {
-        if (j >= lo && j <= hi) {
-          sel = true;
-        } else if (take_all) {
+        if ((j >= r.lo && j <= r.hi) || r.take_all) {
           sel = true;
         } else {
-          const uint32_t kk = krow[j];
+          const uint32_t kk = key_of(j0, j);
           if (kk > tau) sel = true;
           else if (kk == tau) eq = true;
         }
@@ -265,7 +247,98 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
       pos += __popc(sm);
     }
     for (int p = pos + lane; p < g.maxl; p += 32) out[p] = -1;
-    if (lane == 0) a.cnt[static_cast<size_t>(h) * g.nq + i] = pos;
+    if (lane == 0) a.cnt[static_cast<size_t>(h) * g.nq + r.i] = pos;
+  };
+  constexpr int kWarps = kRouteThreads / 32;
+  if constexpr (KPL > 0) {
+    // Keys in registers (lane owns blocks lane + 32 m).  The warp's rows
+    // qi = warp + 8 r are searched RI at a time: their bitwise searches are
+    // independent, so their warp reductions overlap.
+    constexpr int RPW = QB / kWarps;
+    constexpr int RI = (KPL <= 16) ? RPW : (RPW < 2 ? RPW : 2);
+    static_assert(RPW % RI == 0, "rows per warp");
+#pragma unroll 1
+    for (int r0 = 0; r0 < RPW; r0 += RI) {
+      Row rw[RI];
+      uint32_t kr[RI][KPL];
+      uint32_t tau[RI];
+      int need[RI];
+#pragma unroll
+      for (int r = 0; r < RI; ++r) {
+        const int qi = warp + kWarps * (r0 + r);
+        rw[r] = row_of(qi);
+        const bool live = rw[r].i < g.nq;
+        if (!live) rw[r].take_all = true;  // nothing to search
+        const float* srow = sc + qi * g.nvk;
+#pragma unroll
+        for (int m = 0; m < KPL; ++m) {
+          const int j = lane + 32 * m;
+          const bool cand = live && j < g.nvk && (j < rw[r].lo || j > rw[r].hi);
+          kr[r][m] = cand ? order_key(srow[j]) : 0u;
+        }
+        tau[r] = 0;
+      }
+      // Largest tau with #{keys >= tau} >= kp, bit by bit.
+#pragma unroll 1
+      for (int bit = 31; bit >= 0; --bit) {
+        unsigned c[RI];
+#pragma unroll
+        for (int r = 0; r < RI; ++r) {
+          const uint32_t t = tau[r] | (1u << bit);
+          c[r] = 0;
+#pragma unroll
+          for (int m = 0; m < KPL; ++m) c[r] += (kr[r][m] >= t) ? 1u : 0u;
+        }
+#pragma unroll
+        for (int r = 0; r < RI; ++r) c[r] = __reduce_add_sync(0xFFFFFFFFu, c[r]);
+#pragma unroll
+        for (int r = 0; r < RI; ++r)
+          if (static_cast<int>(c[r]) >= rw[r].kp) tau[r] |= (1u << bit);
+      }
+      {
+        unsigned c[RI];
+#pragma unroll
+        for (int r = 0; r < RI; ++r) {
+          c[r] = 0;
+#pragma unroll
+          for (int m = 0; m < KPL; ++m) c[r] += (kr[r][m] > tau[r]) ? 1u : 0u;
+        }
+#pragma unroll
+        for (int r = 0; r < RI; ++r) need[r] = rw[r].kp - static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, c[r]));
+      }
+#pragma unroll
+      for (int r = 0; r < RI; ++r) {
+        if (rw[r].i >= g.nq) continue;
+        const float* srow = sc + (warp + kWarps * (r0 + r)) * g.nvk;
+        emit_row(rw[r], tau[r], need[r], [&](int, int j) { return order_key(srow[j]); });
+      }
+    }
+  } else {
+    // Keys in shared memory (long rows), one row at a time.
+    for (int qi = warp; qi < QB; qi += kWarps) {
+      const Row rw = row_of(qi);
+      if (rw.i >= g.nq) break;
+      uint32_t* krow = reinterpret_cast<uint32_t*>(sc + qi * g.nvk);
+      for (int j = lane; j < g.nvk; j += 32) {
+        const float f = __uint_as_float(krow[j]);
+        krow[j] = (j >= rw.lo && j <= rw.hi) ? 0u : order_key(f);
+      }
+      __syncwarp();
+      uint32_t tau = 0;
+      int need = 0;
+      if (!rw.take_all) {
+        for (int bit = 31; bit >= 0; --bit) {
+          const uint32_t t = tau | (1u << bit);
+          unsigned c = 0;
+          for (int j = lane; j < g.nvk; j += 32) c += (krow[j] >= t) ? 1u : 0u;
+          if (static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, c)) >= rw.kp) tau = t;
+        }
+        unsigned c = 0;
+        for (int j = lane; j < g.nvk; j += 32) c += (krow[j] > tau) ? 1u : 0u;
+        need = rw.kp - static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, c));
+      }
+      emit_row(rw, tau, need, [&](int, int j) { return krow[j]; });
+    }
   }
 }
 
@@ -281,7 +354,7 @@ int route_qb(const Geometry& g) {
 size_t route_topk_smem_bytes(const Geometry& g) {
   const int qb = route_qb(g);
   return sizeof(float) * (static_cast<size_t>(kHeadDim) * qb + kKeyChunk * kKcStride +
-                          static_cast<size_t>(qb) * g.nvk + (kRouteThreads / 32) * 256);
+                          static_cast<size_t>(qb) * g.nvk);
 }
 
 cudaError_t launch_pool(const PlanArgs& a, cudaStream_t s) {
@@ -292,9 +365,9 @@ cudaError_t launch_pool(const PlanArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int QB, int QPT, int KPT>
+template <int QB, int QPT, int KPT, int KPL>
 static cudaError_t launch_route_variant(const PlanArgs& a, size_t smem, cudaStream_t s) {
-  auto* k = route_topk_kernel<QB, QPT, KPT>;
+  auto* k = route_topk_kernel<QB, QPT, KPT, KPL>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const dim3 grid((a.g.nq + QB - 1) / QB, a.g.H);
@@ -305,10 +378,13 @@ static cudaError_t launch_route_variant(const PlanArgs& a, size_t smem, cudaStre
 cudaError_t launch_route_topk(const PlanArgs& a, cudaStream_t s) {
   const size_t smem = route_topk_smem_bytes(a.g);
   switch (route_qb(a.g)) {
-    case 32: return launch_route_variant<32, 8, 2>(a, smem, s);
-    case 16: return launch_route_variant<16, 4, 2>(a, smem, s);
-    case 8: return launch_route_variant<8, 4, 1>(a, smem, s);
-    default: return launch_route_variant<4, 2, 1>(a, smem, s);
+    case 32:
+      if (a.g.nvk <= 256) return launch_route_variant<32, 8, 2, 8>(a, smem, s);
+      if (a.g.nvk <= 512) return launch_route_variant<32, 8, 2, 16>(a, smem, s);
+      return launch_route_variant<32, 8, 2, 32>(a, smem, s);
+    case 16: return launch_route_variant<16, 4, 2, 0>(a, smem, s);
+    case 8: return launch_route_variant<8, 4, 1, 0>(a, smem, s);
+    default: return launch_route_variant<4, 2, 1, 0>(a, smem, s);
   }
 }
 
