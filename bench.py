@@ -174,6 +174,26 @@ def oracle_timing(pool, arrays, prm, heads_per_task, ncores, heads):
     return sum(r[0] for r in res), wall
 
 
+# ----------------------------------------------------------------- ranks
+def max_over_ranks(x, world, device):
+    """The largest of every rank's `x` (a float); the identity on one rank.
+    The job's time is its slowest rank's."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(kept_flop_per_rank, ms_per_step, world):
+    """Whole-job kept TFLOP/s: every rank runs its own copy of the workload,
+    so the job does `world` copies in the slowest rank's step time."""
+    return world * kept_flop_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 # ----------------------------------------------------------------- main legs
 def host_cores():
     try:
@@ -320,12 +340,9 @@ def run_ours(args, rank, world, local_rank):
     fwd_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(args.steps)]
     if bsr.sparse_attn_last_device_status(ws_fwd, stream) != 0:
         raise RuntimeError("device status error in the timed region")
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * kept / (ms_per_step * 1e-3) / 1e12
+    value = weak_scaling_value(kept, ms_per_step, world)
 
     # ---- end to end through the public API, host buffers
     ho = torch.empty((1, T, H, 128), dtype=torch.bfloat16).pin_memory()
@@ -352,12 +369,8 @@ def run_ours(args, rank, world, local_rank):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * kept / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    e2e_value = weak_scaling_value(kept, e2e_ms, world)
 
     if rank != 0:
         return
