@@ -26,3 +26,4 @@ from .oracle import (  # noqa: F401
     select_topk,
     topk_count,
 )
+from .spark import block_ranges, reweight_bytes, round_to_bf16, spark_reweight  # noqa: F401
