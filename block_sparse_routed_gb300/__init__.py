@@ -9,6 +9,8 @@ Two calls, backed by hand-written CUDA kernels in a C-ABI library:
 * ``sparse_attn_fwd``: exact softmax attention of each video query block over
   its list, dense attention for context rows (and a dense video tail), with
   an optional natural-log key bias on sink keys.
+* ``spark_reweight``: Spark's per-block virtual summaries (softmax-weighted
+  keys and values per anchor and 64-token block, and their log-mass).
 
 This module marshals torch tensors to the C entry points of the same names.
 PyTorch provides device memory and streams only; every step runs in the
@@ -27,6 +29,7 @@ from ._native import (  # noqa: F401
     SA_EUNSUPPORTED,
     SA_OK,
     SaParams,
+    SaReweightParams,
     SaSizes,
     SparseAttnError,
     load_library,
@@ -43,6 +46,7 @@ __all__ = [
     "sparse_attn_plan",
     "sparse_attn_query",
     "sparse_attn_status_string",
+    "spark_reweight",
 ]
 
 
@@ -191,3 +195,40 @@ def sparse_attn(params: Params, q, k, v, key_bias=None, check_status=True, strea
         if st != SA_OK:
             raise SparseAttnError(st, "sparse_attn (device)")
     return o
+
+
+def spark_reweight(a, k, v, ak=None, av=None, lm=None, stream=None):
+    """Spark virtual summaries of every (anchor, head, 64-token block).
+
+    a: bf16 [1, P, H, 128] anchors; k, v: bf16 [1, T, H, 128] (CUDA,
+    contiguous).  Returns (ak, av) bf16 [1, P, H, ceil(T/64), 128] and
+    lm float32 [1, P, H, ceil(T/64)], written by the library's kernel.
+    """
+    torch = _torch()
+    for t, n in ((a, "a"), (k, "k"), (v, "v")):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{n} must be a contiguous 4-D CUDA bfloat16 tensor")
+    _, P, H, D = a.shape
+    B, T, Hk, Dk = k.shape
+    if tuple(v.shape) != tuple(k.shape) or Hk != H or Dk != D or a.shape[0] != B:
+        raise ValueError("a [1, P, H, 128], k and v [1, T, H, 128] required")
+    nblk = (T + 63) // 64
+    dev = k.device
+    if ak is None:
+        ak = torch.empty((B, P, H, nblk, D), dtype=torch.bfloat16, device=dev)
+    if av is None:
+        av = torch.empty((B, P, H, nblk, D), dtype=torch.bfloat16, device=dev)
+    if lm is None:
+        lm = torch.empty((B, P, H, nblk), dtype=torch.float32, device=dev)
+    for t, n, dt, want in ((ak, "ak", torch.bfloat16, B * P * H * nblk * D),
+                           (av, "av", torch.bfloat16, B * P * H * nblk * D),
+                           (lm, "lm", torch.float32, B * P * H * nblk)):
+        if t.dtype != dt or not t.is_contiguous() or t.numel() != want or not t.is_cuda:
+            raise ValueError(f"{n}: contiguous CUDA {dt} tensor with {want} elements required")
+    cp = SaReweightParams(_native.SA_ABI_VERSION, B, T, H, D, P)
+    st = _native.sparse_attn_spark_reweight(cp, a.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                            ak.data_ptr(), av.data_ptr(), lm.data_ptr(),
+                                            _stream_handle(stream))
+    if st != SA_OK:
+        raise SparseAttnError(st, "sparse_attn_spark_reweight")
+    return ak, av, lm

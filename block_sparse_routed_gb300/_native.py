@@ -29,6 +29,7 @@ ENTRY_POINTS = (
     "sparse_attn_plan",
     "sparse_attn_plan_static",
     "sparse_attn_fwd",
+    "sparse_attn_spark_reweight",
     "sparse_attn_last_device_status",
     "sparse_attn_last_cuda_error",
     "sparse_attn_status_string",
@@ -61,6 +62,17 @@ class SaSizes(ctypes.Structure):
         ("dense_row_start", ctypes.c_int32),
         ("plan_ws_bytes", ctypes.c_uint64),
         ("fwd_ws_bytes", ctypes.c_uint64),
+    ]
+
+
+class SaReweightParams(ctypes.Structure):
+    _fields_ = [
+        ("abi_version", ctypes.c_uint32),
+        ("B", ctypes.c_int32),
+        ("T", ctypes.c_int32),
+        ("H", ctypes.c_int32),
+        ("D", ctypes.c_int32),
+        ("P", ctypes.c_int32),
     ]
 
 
@@ -102,6 +114,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sparse_attn_last_device_status.restype = ctypes.c_int
     lib.sparse_attn_last_cuda_error.argtypes = [P(ctypes.c_char_p)]
     lib.sparse_attn_last_cuda_error.restype = ctypes.c_int
+    lib.sparse_attn_spark_reweight.argtypes = [P(SaReweightParams), vp, vp, vp, vp, vp, vp, vp]
+    lib.sparse_attn_spark_reweight.restype = ctypes.c_int
     lib.sparse_attn_status_string.argtypes = [ctypes.c_int]
     lib.sparse_attn_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -143,6 +157,12 @@ def sparse_attn_fwd(params, q, k, v, key_bias, idx, cnt, o, ws, ws_bytes, stream
     return load_library().sparse_attn_fwd(
         ctypes.byref(params), q, k, v, key_bias or None, idx, cnt, o, ws, ws_bytes, stream or None
     )
+
+
+def sparse_attn_spark_reweight(params, a, k, v, ak, av, lm, stream) -> int:
+    """Raw call of the virtual-summary entry point.  Returns the status."""
+    return load_library().sparse_attn_spark_reweight(ctypes.byref(params), a, k, v, ak, av, lm,
+                                                     stream or None)
 
 
 def sparse_attn_last_device_status(ws, stream) -> int:

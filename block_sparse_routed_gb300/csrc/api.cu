@@ -219,6 +219,38 @@ SA_API sa_status sparse_attn_fwd(const sa_params* p, const void* q, const void* 
   return SA_OK;
 }
 
+SA_API sa_status sparse_attn_spark_reweight(const sa_reweight_params* p, const void* a, const void* k,
+                                            const void* v, void* ak, void* av, float* lm,
+                                            cudaStream_t stream) {
+  if (p == nullptr) return SA_EINVAL;
+  if (p->abi_version != SA_ABI_VERSION) return SA_EINVAL;
+  if (p->B != 1 || p->D != kHeadDim) return SA_EUNSUPPORTED;
+  if (p->T < 1 || p->H < 1 || p->P < 1) return SA_EINVAL;
+  const int64_t nblk = (static_cast<int64_t>(p->T) + kBlock - 1) / kBlock;
+  const int64_t lim = int64_t(1) << 31;
+  if (int64_t(p->T) * p->H * kHeadDim >= lim || int64_t(p->P) * p->H * nblk * kHeadDim >= lim)
+    return SA_EUNSUPPORTED;
+  if (!a || !k || !v || !ak || !av || !lm) return SA_EINVAL;
+  if (!aligned(a, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(ak, 16) ||
+      !aligned(av, 16) || !aligned(lm, 4))
+    return SA_EINVAL;
+  const sa_status st = check_device();
+  if (st != SA_OK) return st;
+  ReweightArgs r;
+  r.a = static_cast<const uint16_t*>(a);
+  r.k = static_cast<const uint16_t*>(k);
+  r.v = static_cast<const uint16_t*>(v);
+  r.ak = static_cast<uint16_t*>(ak);
+  r.av = static_cast<uint16_t*>(av);
+  r.lm = lm;
+  r.T = p->T;
+  r.H = p->H;
+  r.P = p->P;
+  r.nblk = static_cast<int>(nblk);
+  if (cuda_failed(launch_spark_reweight(r, stream))) return SA_ECUDA;
+  return SA_OK;
+}
+
 SA_API sa_status sparse_attn_last_device_status(const void* ws, cudaStream_t stream,
                                                 sa_status* out) {
   if (!ws || !out) return SA_EINVAL;

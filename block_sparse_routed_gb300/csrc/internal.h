@@ -53,6 +53,16 @@ struct AttnArgs {
   float scale_log2;    // log2(e) / sqrt(128)
 };
 
+struct ReweightArgs {
+  const uint16_t* a;   // BF16 anchors [P, H, 128]
+  const uint16_t* k;   // BF16 [T, H, 128]
+  const uint16_t* v;
+  uint16_t* ak;        // BF16 [P, H, nblk, 128]
+  uint16_t* av;
+  float* lm;           // [P, H, nblk]
+  int T, H, P, nblk;
+};
+
 // Launchers (defined in the kernel translation units).
 cudaError_t launch_pool(const PlanArgs& a, cudaStream_t s);
 cudaError_t launch_route_topk(const PlanArgs& a, cudaStream_t s);
@@ -60,6 +70,7 @@ cudaError_t launch_bias_prep(const float* bias, float* b2, int32_t* status, cons
                              cudaStream_t s);
 cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                              const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_spark_reweight(const ReweightArgs& r, cudaStream_t s);
 size_t route_topk_smem_bytes(const Geometry& g);
 size_t attention_smem_bytes();
 

@@ -1,0 +1,151 @@
+// Spark virtual summaries (spark_reweight) for sm_103a.
+//
+// What is computed ("Sol-Attn and Spark for MiniMax-H3", section "Spark
+// primitives"; default numerics from section "Spark inference integration"):
+// for every anchor a_p (a query representative of head h) and physical
+// 64-token block b of K/V, over the block's real keys u (a partial last block
+// has fewer),
+//     s_u = a_p . k_u / sqrt(128),  w = softmax_u(s)
+//     ak  = sum_u w_u k_u,  av = sum_u w_u v_u              stored as BF16
+//     lm  = logsumexp_u(s_u) - a_p . ak / sqrt(128)          FP32
+// where the ak in lm is the stored BF16 one.
+//
+// The work is one pass over K and V (HBM-bound for a few anchors).  One warp
+// takes one (block, head) pair, consecutive warps the heads of one block so
+// that they read adjacent 256-byte row segments.  Lane l owns dimensions
+// 4l..4l+3 of every row (8-byte loads, one 256-byte row per warp load).
+//   pass 1: each lane forms its 4-dimension partial products for all 64 keys;
+//           a butterfly over 5 lane distances (62 shuffles) leaves lane l with
+//           the full dot products of keys 2l and 2l+1;
+//           block maximum and sum of 2^((d - dmax) log2(e)/sqrt(128)) by warp
+//           reductions;
+//   pass 2: each lane accumulates w_u k_u and w_u v_u over its 4 dimensions,
+//           the weights broadcast by shuffle; the K rows come back from L1/L2.
+#include <cstdint>
+
+#include "internal.h"
+
+namespace sa {
+namespace {
+
+constexpr int kRwWarps = 8;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kInvSqrtD = 0.08838834764831845f;  // 1/sqrt(128)
+
+__device__ __forceinline__ void bf16x4(uint2 w, float (&f)[4]) {
+  f[0] = __uint_as_float(w.x << 16);
+  f[1] = __uint_as_float(w.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(w.y << 16);
+  f[3] = __uint_as_float(w.y & 0xFFFF0000u);
+}
+
+// Round-to-nearest-even FP32 -> BF16 pair (lo in the low half).
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+  return x;
+}
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+  return x;
+}
+
+// One butterfly stage: 2N values per lane -> N, lanes with bit `o` set keep
+// the upper half of the keys.
+template <int N>
+__device__ __forceinline__ void fold(float* v, int lane, int o) {
+  const bool upper = (lane & o) != 0;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const float send = upper ? v[i] : v[i + N];
+    const float keep = upper ? v[i + N] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+  }
+}
+
+__global__ void __launch_bounds__(32 * kRwWarps) spark_reweight_kernel(const ReweightArgs r) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t item = static_cast<int64_t>(blockIdx.x) * kRwWarps + warp;
+  if (item >= static_cast<int64_t>(r.nblk) * r.H) return;
+  const int b = static_cast<int>(item / r.H), h = static_cast<int>(item % r.H);
+  const int u0 = b * kBlock;
+  const int n = min(kBlock, r.T - u0);
+  const size_t stride = static_cast<size_t>(r.H) * (kHeadDim / 4);  // row stride in uint2
+  const uint2* krow = reinterpret_cast<const uint2*>(r.k) + (static_cast<size_t>(u0) * r.H + h) * (kHeadDim / 4) + lane;
+  const uint2* vrow = reinterpret_cast<const uint2*>(r.v) + (static_cast<size_t>(u0) * r.H + h) * (kHeadDim / 4) + lane;
+
+  for (int p = 0; p < r.P; ++p) {
+    float a[4];
+    bf16x4(__ldg(reinterpret_cast<const uint2*>(r.a) + (static_cast<size_t>(p) * r.H + h) * (kHeadDim / 4) + lane), a);
+    // pass 1: partial dot products of this lane's 4 dimensions, every key
+    float d[kBlock];
+#pragma unroll
+    for (int u = 0; u < kBlock; ++u) {
+      d[u] = 0.f;
+      if (u < n) {
+        float kf[4];
+        bf16x4(__ldg(krow + u * stride), kf);
+        d[u] = fmaf(a[3], kf[3], fmaf(a[2], kf[2], fmaf(a[1], kf[1], a[0] * kf[0])));
+      }
+    }
+    fold<32>(d, lane, 16);
+    fold<16>(d, lane, 8);
+    fold<8>(d, lane, 4);
+    fold<4>(d, lane, 2);
+    fold<2>(d, lane, 1);
+    // lane l now holds the dot products of keys 2l and 2l+1
+    const bool ok0 = 2 * lane < n, ok1 = 2 * lane + 1 < n;
+    const float dmax = warp_max(fmaxf(ok0 ? d[0] : -INFINITY, ok1 ? d[1] : -INFINITY));
+    const float c = kLog2e * kInvSqrtD;
+    const float e0 = ok0 ? exp2f((d[0] - dmax) * c) : 0.f;
+    const float e1 = ok1 ? exp2f((d[1] - dmax) * c) : 0.f;
+    const float l = warp_sum(e0 + e1);
+    // pass 2: weighted keys and values over this lane's dimensions
+    float ak[4] = {0.f, 0.f, 0.f, 0.f}, av[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int u = 0; u < n; ++u) {
+      const float w = __shfl_sync(0xFFFFFFFFu, (u & 1) ? e1 : e0, u >> 1);
+      float kf[4], vf[4];
+      bf16x4(__ldg(krow + u * stride), kf);
+      bf16x4(__ldg(vrow + u * stride), vf);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        ak[t] = fmaf(w, kf[t], ak[t]);
+        av[t] = fmaf(w, vf[t], av[t]);
+      }
+    }
+    const float inv_l = 1.0f / l;
+    uint2 ko, vo;
+    ko.x = pack_bf16(ak[0] * inv_l, ak[1] * inv_l);
+    ko.y = pack_bf16(ak[2] * inv_l, ak[3] * inv_l);
+    vo.x = pack_bf16(av[0] * inv_l, av[1] * inv_l);
+    vo.y = pack_bf16(av[2] * inv_l, av[3] * inv_l);
+    const size_t orow = ((static_cast<size_t>(p) * r.H + h) * r.nblk + b);
+    reinterpret_cast<uint2*>(r.ak)[orow * (kHeadDim / 4) + lane] = ko;
+    reinterpret_cast<uint2*>(r.av)[orow * (kHeadDim / 4) + lane] = vo;
+    // log-mass against the stored (rounded) summary key
+    float kr[4];
+    bf16x4(ko, kr);
+    const float key = warp_sum(fmaf(a[3], kr[3], fmaf(a[2], kr[2], fmaf(a[1], kr[1], a[0] * kr[0]))));
+    if (lane == 0) r.lm[orow] = (dmax - key) * kInvSqrtD + logf(l);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_spark_reweight(const ReweightArgs& r, cudaStream_t s) {
+  const int64_t items = static_cast<int64_t>(r.nblk) * r.H;
+  const int64_t grid = (items + kRwWarps - 1) / kRwWarps;
+  if (grid == 0) return cudaSuccess;
+  spark_reweight_kernel<<<static_cast<unsigned>(grid), 32 * kRwWarps, 0, s>>>(r);
+  return cudaGetLastError();
+}
+
+}  // namespace sa

@@ -170,6 +170,40 @@ sa_status sparse_attn_plan_static(const sa_params* p, const void* q, const void*
                                   int32_t* cnt, float* route_scores, cudaStream_t stream);
 
 /*
+ * Spark virtual summaries ("Sol-Attn and Spark for MiniMax-H3", section
+ * "Spark primitives", spark_reweight; default numerics from section "Spark
+ * inference integration").  For every anchor p, head h and physical 64-token
+ * block b of K/V (a partial last block uses only its T - 64 b real keys):
+ *     s_u = a[p, h] . k[u, h] / sqrt(128),   w = softmax over the block's u
+ *     ak[p, h, b] = sum_u w_u k[u, h]        BF16 (round to nearest even)
+ *     av[p, h, b] = sum_u w_u v[u, h]        BF16
+ *     lm[p, h, b] = logsumexp_u(s_u) - a[p, h] . ak[p, h, b] / sqrt(128)
+ * where the ak in lm is the stored BF16 value.  Scores, weights and sums are
+ * FP32.  It does not choose anchors, routes or merge outputs.
+ *   a        BF16 [1, P, H, 128] anchors (query representatives)
+ *   k, v     BF16 [1, T, H, 128]
+ *   ak, av   BF16 [1, P, H, nblk, 128], nblk = ceil(T / 64)
+ *   lm       float32 [1, P, H, nblk]
+ * Errors before launch: SA_EINVAL (null params or tensor pointer,
+ * abi_version mismatch, T < 1, H < 1, P < 1, a tensor pointer not 16-byte
+ * aligned, lm not 4-byte aligned); SA_EUNSUPPORTED (B != 1, D != 128,
+ * T * H * 128 or P * H * nblk * 128 beyond 2^31 elements, a device that is
+ * not sm_103).  SA_ECUDA if the launch fails.  Nothing is device-detected.
+ */
+typedef struct sa_reweight_params {
+  uint32_t abi_version; /* must be SA_ABI_VERSION                               */
+  int32_t B;            /* batch, must be 1                                     */
+  int32_t T;            /* tokens of K and V, >= 1                              */
+  int32_t H;            /* heads, >= 1                                          */
+  int32_t D;            /* head dimension, must be 128                          */
+  int32_t P;            /* anchors per head, >= 1                               */
+} sa_reweight_params;
+
+sa_status sparse_attn_spark_reweight(const sa_reweight_params* p, const void* a, const void* k,
+                                     const void* v, void* ak, void* av, float* lm,
+                                     cudaStream_t stream);
+
+/*
  * Reads the device status word of `ws` (written by the last plan or fwd
  * enqueued with it).  Synchronises `stream`.  SA_ECUDA if the copy fails.
  */

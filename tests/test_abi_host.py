@@ -169,3 +169,33 @@ def test_python_binding_checks_key_bias_before_the_call(native):
         # CPU tensors are rejected before anything reaches the library
         bsr.sparse_attn_fwd(p, *(torch.zeros(1, 1152, 2, 128, dtype=torch.bfloat16),) * 3,
                             idx=None, cnt=None, key_bias=torch.zeros(1152))
+
+
+def test_spark_reweight_rejects_bad_arguments_before_launch(native):
+    """Argument errors of the virtual-summary entry point, all caught on the
+    host (this host has no GPU: reaching the device would give SA_ECUDA or
+    SA_EUNSUPPORTED from the device check instead)."""
+    assert ctypes.sizeof(native.SaReweightParams) == 24
+    lib = native.load_library()
+    E, U = native.SA_EINVAL, native.SA_EUNSUPPORTED
+    A = 1 << 20
+
+    def call(p, a=A, k=A, v=A, ak=A, av=A, lm=A):
+        return lib.sparse_attn_spark_reweight(ctypes.byref(p), a, k, v, ak, av, lm, None)
+
+    def params(B=1, T=100, H=2, D=128, P=1, ver=None):
+        return native.SaReweightParams(native.SA_ABI_VERSION if ver is None else ver, B, T, H, D, P)
+
+    assert lib.sparse_attn_spark_reweight(None, A, A, A, A, A, A, None) == E
+    assert call(params(ver=3)) == E
+    assert call(params(B=2)) == U
+    assert call(params(D=64)) == U
+    assert call(params(T=0)) == E
+    assert call(params(H=0)) == E
+    assert call(params(P=0)) == E
+    assert call(params(T=1 << 20, H=32)) == U   # 2^32 elements
+    assert call(params(), a=None) == E
+    assert call(params(), lm=None) == E
+    assert call(params(), k=A + 8) == E
+    assert call(params(), ak=A + 2) == E
+    assert call(params(), lm=A + 2) == E

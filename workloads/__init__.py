@@ -7,9 +7,12 @@ arrays it returns.
 """
 
 from .synth import (  # noqa: F401
+    REWEIGHT_WORKLOADS,
     WORKLOADS,
     Workload,
     bf16_round_bits,
+    make_anchors,
     make_inputs,
+    make_reweight_workload,
     make_workload,
 )

@@ -184,3 +184,30 @@ def make_workload(name: str):
         tail_mode=w.tail_mode,
     )
     return arrays, params
+
+
+# Virtual-summary (spark_reweight) workloads: the K/V of an attention workload
+# plus P anchors per head.  The anchors stand in for query representatives
+# (the page's default is one per head); they are drawn N(0, scale^2) per
+# dimension and rounded to BF16, from their own PCG64 stream.
+REWEIGHT_WORKLOADS = {
+    # name: (attention workload for K/V, anchors per head, anchor scale, seed)
+    "reweight_h3": ("h3", 1, 1.0, 11),
+    "reweight_h3_p4": ("h3", 4, 1.0, 12),
+    "reweight_32k": ("32k", 1, 1.0, 13),
+    "reweight_8k_sharp": ("8k", 2, 4.0, 14),
+}
+
+
+def make_anchors(P: int, H: int, scale: float, seed: int) -> np.ndarray:
+    """BF16 bits [P, H, 128] of N(0, scale^2) anchors."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return bf16_round_bits(rng.standard_normal((P, H, D_HEAD), dtype=np.float32) * np.float32(scale))
+
+
+def make_reweight_workload(name: str):
+    """(k, v, a) BF16 bits and the sizes of one named reweight workload."""
+    base, P, scale, seed = REWEIGHT_WORKLOADS[name]
+    arrays, prm = make_workload(base)
+    a = make_anchors(P, prm["H"], scale, seed)
+    return {"k": arrays["k"], "v": arrays["v"], "a": a}, dict(T=prm["T"], H=prm["H"], P=P, base=base)
