@@ -11,6 +11,12 @@ The metric is kept-block attention TFLOP/s: 4 * 128 FLOP per (real query
 row, kept key) pair, summed over heads, divided by the step time.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py --op reweight      # Spark virtual summaries instead
+
+``--op reweight`` measures the second operation of the library, the Spark
+virtual summaries (sparse_attn_spark_reweight) over the same H3-shaped K/V
+with one anchor per head: HBM bytes per second against the measured copy
+bandwidth (K and V read once; summaries written).
 
 Rank 0 prints one JSON line.  With N > 1 (torchrun), every rank runs its own
 independent copy of the workload (weak scaling: heads and problems are
@@ -425,6 +431,144 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def _reweight_worker(args):
+    a, k, v = args
+    import oracle as O
+
+    t0 = time.perf_counter()
+    O.spark_reweight(a, k, v)
+    return time.perf_counter() - t0
+
+
+def reweight_bytes(P, T, H):
+    nblk = (T + 63) // 64
+    return 2 * T * H * 256 + P * H * 256 + P * H * nblk * (2 * 256 + 4)
+
+
+def run_reweight(args, rank, world, local_rank):
+    """Spark virtual summaries: algorithmic HBM bytes per second."""
+    import torch
+
+    import block_sparse_routed_gb300 as bsr
+    from workloads import make_reweight_workload
+
+    name = "reweight_h3"
+    arrays, prm = make_reweight_workload(name)
+    T, H, P = prm["T"], prm["H"], prm["P"]
+    nblk = (T + 63) // 64
+    pool = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        pool = _oracle_pool(host_cores())
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    bsr.load_library()
+
+    def pinned(bits, shape):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).reshape(shape).pin_memory()
+
+    ha, hk, hv = pinned(arrays["a"], (1, P, H, 128)), pinned(arrays["k"], (1, T, H, 128)), pinned(arrays["v"], (1, T, H, 128))
+    a, k, v = ha.to(dev), hk.to(dev), hv.to(dev)
+    ak = torch.empty((1, P, H, nblk, 128), dtype=torch.bfloat16, device=dev)
+    av = torch.empty_like(ak)
+    lm = torch.empty((1, P, H, nblk), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        bsr.spark_reweight(a, k, v, ak=ak, av=av, lm=lm, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    nbytes = reweight_bytes(P, T, H)
+    clocks = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for e0, e1 in ev:
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    per = [e0.elapsed_time(e1) for e0, e1 in ev]
+    ms = max_over_ranks(sum(per) / len(per), world, dev)
+    value = world * nbytes / (ms * 1e-3) / 1e9
+
+    hak = torch.empty((1, P, H, nblk, 128), dtype=torch.bfloat16).pin_memory()
+    hav = torch.empty_like(hak).pin_memory()
+    hlm = torch.empty((1, P, H, nblk), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        a.copy_(ha, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        step()
+        hak.copy_(ak, non_blocking=True)
+        hav.copy_(av, non_blocking=True)
+        hlm.copy_(lm, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    if rank != 0:
+        return
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks["hbm_gbs"])
+    cpu = None
+    if pool is not None:
+        try:
+            hs = list(range(min(H, host_cores())))
+            tasks = [(np.ascontiguousarray(arrays["a"][:, [h]]), np.ascontiguousarray(arrays["k"][:, [h]]),
+                      np.ascontiguousarray(arrays["v"][:, [h]])) for h in hs]
+            t0 = time.perf_counter()
+            pool.map(_reweight_worker, tasks, chunksize=1)
+            secs = time.perf_counter() - t0
+            cpu = {"value": reweight_bytes(P, T, len(hs)) / secs / 1e9, "unit": "GB/s", "cores": host_cores(),
+                   "kind": "oracle", "seconds": secs,
+                   "sample": f"{len(hs)} of {H} heads, all blocks, one head per task"}
+        finally:
+            pool.close()
+            pool.join()
+    line = {
+        "metric": "spark_reweight HBM GB/s (virtual summaries, H3-shaped K/V, 1 anchor per head)",
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "Spark virtual summaries over H3-shaped K/V (9505 tokens x 56 heads), "
+                               "1 anchor per head", "T": T, "H": H, "P": P, "blocks": nblk,
+                   "l2": "K+V 272 MB > 126 MB L2, no flush"},
+        "roofline": {"bound": "hbm", "achieved": value, "peak": peak, "unit": "GB/s", "frac": value / peak,
+                     "traffic": None, "kernel": "spark_reweight_kernel",
+                     "peak_kind": f"{peak_kind} copy bandwidth"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": (2 * T * H + P * H) * 256,
+                "d2h_bytes_per_step": P * H * nblk * (2 * 256 + 4), "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -432,6 +576,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["attention", "reweight"], default="attention")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -446,7 +591,10 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     try:
-        run_ours(args, rank, world, local_rank)
+        if args.op == "reweight":
+            run_reweight(args, rank, world, local_rank)
+        else:
+            run_ours(args, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

@@ -14,13 +14,14 @@
 // takes one (block, head) pair, consecutive warps the heads of one block so
 // that they read adjacent 256-byte row segments.  Lane l owns dimensions
 // 4l..4l+3 of every row (8-byte loads, one 256-byte row per warp load).
-//   pass 1: each lane forms its 4-dimension partial products for all 64 keys;
-//           a butterfly over 5 lane distances (62 shuffles) leaves lane l with
-//           the full dot products of keys 2l and 2l+1;
-//           block maximum and sum of 2^((d - dmax) log2(e)/sqrt(128)) by warp
+//   pass 1: for each half of the block (32 keys) each lane forms its
+//           4-dimension partial products; a butterfly over 5 lane distances
+//           (31 shuffles) leaves lane l with the full dot product of key l of
+//           that half.  Meanwhile the V rows are prefetched into L2.  Block
+//           maximum and sum of 2^((d - dmax) log2(e)/sqrt(128)) by warp
 //           reductions;
 //   pass 2: each lane accumulates w_u k_u and w_u v_u over its 4 dimensions,
-//           the weights broadcast by shuffle; the K rows come back from L1/L2.
+//           the weights broadcast by shuffle; the K rows come back from L2.
 #include <cstdint>
 
 #include "internal.h"
@@ -70,7 +71,7 @@ __device__ __forceinline__ void fold(float* v, int lane, int o) {
   }
 }
 
-__global__ void __launch_bounds__(32 * kRwWarps) spark_reweight_kernel(const ReweightArgs r) {
+__global__ void __launch_bounds__(32 * kRwWarps, 2) spark_reweight_kernel(const ReweightArgs r) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int64_t item = static_cast<int64_t>(blockIdx.x) * kRwWarps + warp;
   if (item >= static_cast<int64_t>(r.nblk) * r.H) return;
@@ -84,41 +85,67 @@ __global__ void __launch_bounds__(32 * kRwWarps) spark_reweight_kernel(const Rew
   for (int p = 0; p < r.P; ++p) {
     float a[4];
     bf16x4(__ldg(reinterpret_cast<const uint2*>(r.a) + (static_cast<size_t>(p) * r.H + h) * (kHeadDim / 4) + lane), a);
-    // pass 1: partial dot products of this lane's 4 dimensions, every key
-    float d[kBlock];
+    // pass 1: per half, partial dot products of this lane's 4 dimensions
+    float dk[2];
 #pragma unroll
-    for (int u = 0; u < kBlock; ++u) {
-      d[u] = 0.f;
-      if (u < n) {
-        float kf[4];
-        bf16x4(__ldg(krow + u * stride), kf);
-        d[u] = fmaf(a[3], kf[3], fmaf(a[2], kf[2], fmaf(a[1], kf[1], a[0] * kf[0])));
+    for (int hf = 0; hf < 2; ++hf) {
+      // all 32 row loads of the half are issued before any is used
+      uint2 kw[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int u = 32 * hf + i;
+        kw[i] = (u < n) ? __ldg(krow + u * stride) : make_uint2(0u, 0u);
       }
+      if (p == 0) {
+#pragma unroll 4
+        for (int i = 0; i < 32; ++i)
+          if (32 * hf + i < n) asm volatile("prefetch.global.L2 [%0];" ::"l"(vrow + (32 * hf + i) * stride));
+      }
+      float d[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float kf[4];
+        bf16x4(kw[i], kf);
+        d[i] = fmaf(a[3], kf[3], fmaf(a[2], kf[2], fmaf(a[1], kf[1], a[0] * kf[0])));
+      }
+      fold<16>(d, lane, 16);
+      fold<8>(d, lane, 8);
+      fold<4>(d, lane, 4);
+      fold<2>(d, lane, 2);
+      fold<1>(d, lane, 1);
+      dk[hf] = d[0];  // key 32 hf + lane
     }
-    fold<32>(d, lane, 16);
-    fold<16>(d, lane, 8);
-    fold<8>(d, lane, 4);
-    fold<4>(d, lane, 2);
-    fold<2>(d, lane, 1);
-    // lane l now holds the dot products of keys 2l and 2l+1
-    const bool ok0 = 2 * lane < n, ok1 = 2 * lane + 1 < n;
-    const float dmax = warp_max(fmaxf(ok0 ? d[0] : -INFINITY, ok1 ? d[1] : -INFINITY));
+    const bool ok0 = lane < n, ok1 = 32 + lane < n;
+    const float dmax = warp_max(fmaxf(ok0 ? dk[0] : -INFINITY, ok1 ? dk[1] : -INFINITY));
     const float c = kLog2e * kInvSqrtD;
-    const float e0 = ok0 ? exp2f((d[0] - dmax) * c) : 0.f;
-    const float e1 = ok1 ? exp2f((d[1] - dmax) * c) : 0.f;
+    const float e0 = ok0 ? exp2f((dk[0] - dmax) * c) : 0.f;
+    const float e1 = ok1 ? exp2f((dk[1] - dmax) * c) : 0.f;
     const float l = warp_sum(e0 + e1);
     // pass 2: weighted keys and values over this lane's dimensions
     float ak[4] = {0.f, 0.f, 0.f, 0.f}, av[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-    for (int u = 0; u < n; ++u) {
-      const float w = __shfl_sync(0xFFFFFFFFu, (u & 1) ? e1 : e0, u >> 1);
-      float kf[4], vf[4];
-      bf16x4(__ldg(krow + u * stride), kf);
-      bf16x4(__ldg(vrow + u * stride), vf);
+    // 16 keys at a time: their 32 row loads are issued before any is used
+#pragma unroll 1
+    for (int u0 = 0; u0 < n; u0 += 16) {
+      uint2 kw[16], vw[16];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        ak[t] = fmaf(w, kf[t], ak[t]);
-        av[t] = fmaf(w, vf[t], av[t]);
+      for (int i = 0; i < 16; ++i) {
+        const bool in = u0 + i < n;
+        kw[i] = in ? __ldg(krow + (u0 + i) * stride) : make_uint2(0u, 0u);
+        vw[i] = in ? __ldg(vrow + (u0 + i) * stride) : make_uint2(0u, 0u);
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int u = u0 + i;
+        // zero weight past the block end (those rows were not loaded)
+        const float w = __shfl_sync(0xFFFFFFFFu, (u < 32) ? e0 : e1, u & 31);
+        float kf[4], vf[4];
+        bf16x4(kw[i], kf);
+        bf16x4(vw[i], vf);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          ak[t] = fmaf(w, kf[t], ak[t]);
+          av[t] = fmaf(w, vf[t], av[t]);
+        }
       }
     }
     const float inv_l = 1.0f / l;
