@@ -26,4 +26,14 @@ from .oracle import (  # noqa: F401
     select_topk,
     topk_count,
 )
-from .spark import block_ranges, reweight_bytes, round_to_bf16, spark_reweight  # noqa: F401
+from .spark import (  # noqa: F401
+    bf16_bits,
+    block_ranges,
+    forward_merged,
+    reweight_bytes,
+    round_to_bf16,
+    skipped_blocks,
+    spark_forward,
+    spark_reweight,
+    video_query_anchor,
+)

@@ -101,3 +101,80 @@ def reweight_bytes(P: int, T: int, H: int) -> int:
     ak/av (BF16) and lm (FP32) written."""
     nb = (T + BLOCK - 1) // BLOCK
     return 2 * T * H * HEAD_DIM * 2 + P * H * HEAD_DIM * 2 + P * H * nb * (2 * HEAD_DIM * 2 + 4)
+
+
+# ---------------------------------------------------------------- merged attention
+# "Sol-Attn and Spark for MiniMax-H3", section "Spark inference integration":
+# one global representative per head, formed by averaging all target-video
+# queries and stored as BF16; global-anchor K/V and log-mass summaries merged
+# with exact attention.  Read here as: every video key block that a sparse
+# query block's list skips enters that block's softmax as one virtual key,
+# the summary key ak, with logit q . ak / sqrt(128) + lm and value av.  For a
+# query equal to the anchor this reproduces the block's exact contribution,
+# since exp(a . ak / sqrt(128) + lm) = sum_u exp(a . k_u / sqrt(128)).
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """BF16 bit patterns of float64 values that are BF16 values."""
+    f = np.asarray(x, dtype=np.float32)
+    u = f.view(np.uint32)
+    assert np.all((u & 0xFFFF) == 0), "not a BF16 value"
+    return (u >> 16).astype(np.uint16)
+
+
+def video_query_anchor(q_bits: np.ndarray, video_tokens: int) -> np.ndarray:
+    """BF16 bits [1, H, 128]: per head the mean of the target-video query
+    rows t < video_tokens, rounded to BF16."""
+    q = decode_bf16(q_bits[:video_tokens])
+    return bf16_bits(round_to_bf16(q.mean(axis=0)))[None]
+
+
+def skipped_blocks(h: int, i: int, idx: np.ndarray, cnt: np.ndarray, nvk: int) -> np.ndarray:
+    """Video key blocks j < nvk absent from the list of query block i, head h."""
+    listed = set(int(b) for b in idx[h, i, : cnt[h, i]])
+    return np.array([j for j in range(nvk) if j not in listed], dtype=np.int64)
+
+
+def forward_merged(q_bits, k_bits, v_bits, bias, idx, cnt, sz, ak, av, lm, heads=None):
+    """Exact attention over each list plus one virtual key per skipped video
+    key block: O [T, len(heads), 128] fp64.
+
+    ak, av: [H, nblk, 128] summaries (one anchor per head), lm: [H, nblk].
+    Dense rows attend every key exactly and see no virtual key.
+    """
+    from .oracle import _softmax_attend, check_key_bias, query_block_rows, row_key_set
+
+    b = check_key_bias(bias, sz)
+    heads = list(range(sz.H)) if heads is None else list(heads)
+    out = np.zeros((sz.T, len(heads), sz.D))
+    for hn, h in enumerate(heads):
+        q = decode_bf16(q_bits[:, h, :])
+        k = decode_bf16(k_bits[:, h, :])
+        v = decode_bf16(v_bits[:, h, :])
+        for i in range(sz.nq):
+            rows = np.arange(query_block_rows(i, sz).start, query_block_rows(i, sz).stop)
+            keys = row_key_set(int(rows[0]), h, idx, cnt, sz)
+            sk = skipped_blocks(h, i, idx, cnt, sz.nvk)
+            # virtual keys after the exact ones; the log-mass is an additive logit
+            kk = np.concatenate([k[keys], ak[h, sk]])
+            vv = np.concatenate([v[keys], av[h, sk]])
+            bb = np.concatenate([b[keys], lm[h, sk]])
+            out[rows, hn] = _softmax_attend(q[rows], kk, vv, bb, sz.D)
+        rows = np.arange(sz.dense_row_start, sz.T)
+        if rows.size:
+            out[rows, hn] = _softmax_attend(q[rows], k, v, b, sz.D)
+    return out
+
+
+def spark_forward(q_bits, k_bits, v_bits, bias, sz, plan_out=None):
+    """The whole merged path: routing lists, the per-head anchor (mean of the
+    video queries), its virtual summaries (stored BF16 values) and the merged
+    attention.  Returns dict(o, idx, cnt, a, ak16, av16, lm)."""
+    from .oracle import plan
+
+    ref = plan_out if plan_out is not None else plan(q_bits, k_bits, sz)
+    a = video_query_anchor(q_bits, sz.Nv)
+    s = spark_reweight(a, k_bits, v_bits)
+    o = forward_merged(q_bits, k_bits, v_bits, bias, ref["idx"], ref["cnt"], sz,
+                       s["ak16"][0], s["av16"][0], s["lm"][0])
+    return {"o": o, "idx": ref["idx"], "cnt": ref["cnt"], "a": a, "ak16": s["ak16"][0],
+            "av16": s["av16"][0], "lm": s["lm"][0]}
