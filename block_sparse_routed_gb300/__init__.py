@@ -11,6 +11,9 @@ Two calls, backed by hand-written CUDA kernels in a C-ABI library:
   an optional natural-log key bias on sink keys.
 * ``spark_reweight``: Spark's per-block virtual summaries (softmax-weighted
   keys and values per anchor and 64-token block, and their log-mass).
+* ``sparse_attn_spark_fwd`` / ``spark_attn``: Spark's merged attention: the
+  exact lists plus one summary key per skipped video block, from a per-head
+  anchor (the mean of the target-video queries).
 
 This module marshals torch tensors to the C entry points of the same names.
 PyTorch provides device memory and streams only; every step runs in the
@@ -46,7 +49,9 @@ __all__ = [
     "sparse_attn_plan",
     "sparse_attn_query",
     "sparse_attn_status_string",
+    "spark_attn",
     "spark_reweight",
+    "sparse_attn_spark_fwd",
 ]
 
 
@@ -232,3 +237,46 @@ def spark_reweight(a, k, v, ak=None, av=None, lm=None, stream=None):
     if st != SA_OK:
         raise SparseAttnError(st, "sparse_attn_spark_reweight")
     return ak, av, lm
+
+
+def sparse_attn_spark_fwd(params: Params, q, k, v, idx, cnt, key_bias=None, o=None, ws=None,
+                          stream=None):
+    """Merged (Spark) attention output o (bf16, same shape as q): the lists'
+    exact keys plus one summary key per skipped video block.  The device
+    status is read with ``sparse_attn_last_device_status(ws)``."""
+    torch = _torch()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_qkv(t, n, params)
+    cp = params.to_c()
+    if key_bias is not None:
+        if (key_bias.dtype != torch.float32 or not key_bias.is_contiguous()
+                or key_bias.numel() != params.B * params.T or not key_bias.is_cuda):
+            raise ValueError("key_bias must be a contiguous CUDA float32 tensor with B*T elements")
+    if o is None:
+        o = torch.empty_like(q)
+    _check_qkv(o, "o", params)
+    nbytes = _native.sparse_attn_spark_ws_bytes(cp)
+    if ws is None:
+        ws = _workspace(nbytes, q.device)
+    st = _native.sparse_attn_spark_fwd(cp, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                       key_bias.data_ptr() if key_bias is not None else 0,
+                                       idx.data_ptr(), cnt.data_ptr(), o.data_ptr(), ws.data_ptr(),
+                                       ws.numel(), _stream_handle(stream))
+    if st != SA_OK:
+        raise SparseAttnError(st, "sparse_attn_spark_fwd")
+    return o
+
+
+def spark_attn(params: Params, q, k, v, key_bias=None, check_status=True, stream=None):
+    """plan + merged forward in one call; raises on a device-detected error
+    when ``check_status`` (which synchronises the stream)."""
+    sz = _native.sparse_attn_query(params.to_c())
+    nbytes = max(sz.plan_ws_bytes, _native.sparse_attn_spark_ws_bytes(params.to_c()))
+    ws = _workspace(nbytes, q.device)
+    idx, cnt = sparse_attn_plan(params, q, k, ws=ws, stream=stream)
+    o = sparse_attn_spark_fwd(params, q, k, v, idx, cnt, key_bias=key_bias, ws=ws, stream=stream)
+    if check_status:
+        st = sparse_attn_last_device_status(ws, stream)
+        if st != SA_OK:
+            raise SparseAttnError(st, "spark_attn (device)")
+    return o

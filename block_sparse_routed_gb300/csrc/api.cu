@@ -124,19 +124,46 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D view [T rows, H*128 columns] of a BF16 [T, H, 128] tensor, box of 64
-// columns (128 bytes, one swizzle row) x box_rows rows, 128-byte swizzle,
-// zero fill past the last row.
-bool make_map(CUtensorMap* m, const void* ptr, const Geometry& g, uint32_t box_rows) {
+// 2-D view [rows, cols] of a row-major BF16 tensor, box of 64 columns (128
+// bytes, one swizzle row) x box_rows rows, 128-byte swizzle, zero fill past
+// the last row.
+bool make_map_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   auto enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(g.H) * kHeadDim, static_cast<cuuint64_t>(g.T)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(g.H) * kHeadDim * 2};
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [T rows, H*128 columns] view of a BF16 [T, H, 128] tensor.
+bool make_map(CUtensorMap* m, const void* ptr, const Geometry& g, uint32_t box_rows) {
+  return make_map_2d(m, ptr, static_cast<uint64_t>(g.T), static_cast<uint64_t>(g.H) * kHeadDim, box_rows);
+}
+
+// Workspace of the merged (Spark) forward, after the 256-byte status area.
+struct SparkLayout {
+  uint64_t b2, anchor, partial, ak, av, lm, lm2, total;
+  int nch, nblkp;
+};
+SparkLayout spark_layout(const Geometry& g) {
+  SparkLayout L;
+  const uint64_t H = g.H, nblk = g.nblk;
+  L.nch = anchor_chunks(g.Nv);
+  L.nblkp = ((g.nvk + kBlock - 1) / kBlock) * kBlock;
+  uint64_t off = kStatusBytes;
+  L.b2 = off;      off += align256(uint64_t(g.T) * 4);
+  L.anchor = off;  off += align256(H * kHeadDim * 2);
+  L.partial = off; off += align256(H * L.nch * kHeadDim * 4);
+  L.ak = off;      off += align256(H * nblk * kHeadDim * 2);
+  L.av = off;      off += align256(H * nblk * kHeadDim * 2);
+  L.lm = off;      off += align256(H * nblk * 4);
+  L.lm2 = off;     off += align256(H * L.nblkp * 4);
+  L.total = off;
+  return L;
 }
 
 }  // namespace
@@ -215,7 +242,93 @@ SA_API sa_status sparse_attn_fwd(const sa_params* p, const void* q, const void* 
   a.n_dense = (g.T - g.r0 + 127) / 128;
   a.n_pairs = (g.nq + 1) / 2;
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(128.0));
-  if (cuda_failed(launch_attention(tq, tk, tv, a, stream))) return SA_ECUDA;
+  a.merged = 0;
+  a.lm2 = nullptr;
+  a.nblkp = 0;
+  // the summary maps are unused without merging
+  if (cuda_failed(launch_attention(tq, tk, tv, tk, tv, a, stream))) return SA_ECUDA;
+  return SA_OK;
+}
+
+SA_API sa_status sparse_attn_spark_ws_bytes(const sa_params* p, uint64_t* out) {
+  if (out == nullptr) return SA_EINVAL;
+  Geometry g;
+  const sa_status st = derive(p, &g, nullptr);
+  if (st != SA_OK) return st;
+  const uint64_t nblk = g.nblk;
+  if (uint64_t(g.H) * nblk * kHeadDim >= (uint64_t(1) << 31)) return SA_EUNSUPPORTED;
+  *out = spark_layout(g).total;
+  return SA_OK;
+}
+
+SA_API sa_status sparse_attn_spark_fwd(const sa_params* p, const void* q, const void* k, const void* v,
+                                       const float* key_bias, const int32_t* idx, const int32_t* cnt,
+                                       void* o, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  Geometry g;
+  sa_sizes sz;
+  sa_status st = derive(p, &g, &sz);
+  if (st != SA_OK) return st;
+  if (uint64_t(g.H) * uint64_t(g.nblk) * kHeadDim >= (uint64_t(1) << 31)) return SA_EUNSUPPORTED;
+  if (!q || !k || !v || !idx || !cnt || !o || !ws) return SA_EINVAL;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(idx, 4) || !aligned(cnt, 4) || !aligned(ws, 256) ||
+      (key_bias && !aligned(key_bias, 4)))
+    return SA_EINVAL;
+  const SparkLayout L = spark_layout(g);
+  if (ws_bytes < L.total) return SA_EINVAL;
+  st = check_device();
+  if (st != SA_OK) return st;
+
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint16_t* anchor = reinterpret_cast<uint16_t*>(w + L.anchor);
+  uint16_t* ak = reinterpret_cast<uint16_t*>(w + L.ak);
+  uint16_t* av = reinterpret_cast<uint16_t*>(w + L.av);
+  float* lm = reinterpret_cast<float*>(w + L.lm);
+  float* lm2 = reinterpret_cast<float*>(w + L.lm2);
+  CUtensorMap tq, tk, tv, tak, tav;
+  if (!make_map(&tq, q, g, 128) || !make_map(&tk, k, g, 64) || !make_map(&tv, v, g, 64) ||
+      !make_map_2d(&tak, ak, uint64_t(g.H) * g.nblk, kHeadDim, 64) ||
+      !make_map_2d(&tav, av, uint64_t(g.H) * g.nblk, kHeadDim, 64))
+    return SA_ECUDA;
+
+  int32_t* status = reinterpret_cast<int32_t*>(w);
+  float* b2 = key_bias ? reinterpret_cast<float*>(w + L.b2) : nullptr;
+  if (cuda_failed(cudaMemsetAsync(ws, 0, kStatusBytes, stream))) return SA_ECUDA;
+  if (key_bias && cuda_failed(launch_bias_prep(key_bias, b2, status, g, stream))) return SA_ECUDA;
+  // the per-head anchor, its summaries of every block, the log-mass in log2
+  if (cuda_failed(launch_video_query_mean(static_cast<const uint16_t*>(q),
+                                          reinterpret_cast<float*>(w + L.partial), anchor, g.H, g.Nv,
+                                          stream)))
+    return SA_ECUDA;
+  ReweightArgs r;
+  r.a = anchor;
+  r.k = static_cast<const uint16_t*>(k);
+  r.v = static_cast<const uint16_t*>(v);
+  r.ak = ak;
+  r.av = av;
+  r.lm = lm;
+  r.T = g.T;
+  r.H = g.H;
+  r.P = 1;
+  r.nblk = g.nblk;
+  if (cuda_failed(launch_spark_reweight(r, stream))) return SA_ECUDA;
+  if (cuda_failed(launch_logmass_log2(lm, lm2, g.H, g.nblk, g.nvk, L.nblkp, stream))) return SA_ECUDA;
+
+  AttnArgs a;
+  a.idx = idx;
+  a.cnt = cnt;
+  a.b2 = b2;
+  a.o = static_cast<uint16_t*>(o);
+  a.status = status;
+  a.unit_counter = status + 1;  // inside the status area, cleared above
+  a.g = g;
+  a.n_dense = (g.T - g.r0 + 127) / 128;
+  a.n_pairs = (g.nq + 1) / 2;
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(128.0));
+  a.merged = 1;
+  a.lm2 = lm2;
+  a.nblkp = L.nblkp;
+  if (cuda_failed(launch_attention(tq, tk, tv, tak, tav, a, stream))) return SA_ECUDA;
   return SA_OK;
 }
 

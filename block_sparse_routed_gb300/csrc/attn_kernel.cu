@@ -75,12 +75,14 @@ constexpr uint32_t kQBytes = 32768;     // Q tile: 2 chunks x [128 rows x 128 B]
 constexpr float kRescaleLog2 = 32.0f;
 
 // Shared-memory layout (bytes from a 1024-aligned base).
-constexpr int kMaxEnt = 2 * kMaxList;
+constexpr int kMaxChunks = kMaxVideoBlocks / kBlock;  // chunks of 64 summary keys
+constexpr int kMaxEnt = 2 * kMaxList + kMaxChunks;
 constexpr uint32_t kOffQ = 0;                                   // 2 Q buffers
 constexpr uint32_t kOffRing = 2 * kQBytes;                      // kSlots x kSlotBytes
 constexpr uint32_t kOffEnt = kOffRing + kSlots * kSlotBytes;    // 2 x kMaxEnt int32
 constexpr uint32_t kOffScratch = kOffEnt + 2 * 4 * kMaxEnt;     // 2 x kMaxList int32 (merge)
-constexpr uint32_t kOffXchg = kOffScratch + 2 * 4 * kMaxList;   // [3][128] refs + [2][128] sums
+constexpr uint32_t kOffMask = kOffScratch + 2 * 4 * kMaxList;   // 2 x [kMaxChunks][2] uint64
+constexpr uint32_t kOffXchg = kOffMask + 2 * 8 * 2 * kMaxChunks; // [3][128] refs + [2][128] sums
 constexpr uint32_t kOffUnit = kOffXchg + 4 * 5 * 128;           // 2 unit descriptors
 constexpr uint32_t kOffBar = kOffUnit + 64;
 constexpr uint32_t kOffMisc = kOffBar + 512;
@@ -120,7 +122,8 @@ struct UnitDesc {
 static_assert(sizeof(UnitDesc) * 2 <= 64, "unit area");
 
 constexpr uint32_t kEntMaskShift = 30;
-constexpr uint32_t kEntBlockMask = (1u << kEntMaskShift) - 1u;
+constexpr uint32_t kEntVirtual = 1u << 29;          // a chunk of 64 summary keys
+constexpr uint32_t kEntBlockMask = kEntVirtual - 1u;
 
 __device__ __forceinline__ int lower_bound_s(const int32_t* a, int n, int32_t x) {
   int lo = 0, hi = n;
@@ -221,9 +224,14 @@ __device__ __forceinline__ void decode_unit(const AttnArgs& a, int u, UnitDesc& 
   }
 }
 
+// kMerged: Spark's merged mode (skipped video blocks enter as summary keys).
+// The exact path is a separate instantiation so that its softmax code stays
+// as compact as it can be.
+template <bool kMerged>
 __global__ void __launch_bounds__(kThreads, 1)
 attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_ak,
+                 const __grid_constant__ CUtensorMap tm_av, const AttnArgs a) {
   const Geometry& g = a.g;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -236,6 +244,9 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   volatile int32_t* s_status = reinterpret_cast<volatile int32_t*>(base + kOffMisc + 24);
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * i; };
   auto ent_buf = [&](int slot) { return reinterpret_cast<int32_t*>(base + kOffEnt + 4u * kMaxEnt * slot); };
+  // keep-masks of the summary keys of a unit: [chunk][row half], bit u set
+  // when video block 64 chunk + u is skipped by that half's list
+  auto vmask = [&](int slot) { return reinterpret_cast<unsigned long long*>(base + kOffMask) + slot * 2 * kMaxChunks; };
 
   if (threadIdx.x == 0) {
     *s_status = *reinterpret_cast<volatile int32_t*>(a.status);
@@ -267,16 +278,18 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   // Entry e of unit `d` (descriptor slot `slot`): block index and row-half
   // mask (bit 0: rows 0-63, bit 1: rows 64-127).  An odd count is padded with
   // a masked copy of the last entry so every step loads two real blocks.
-  auto entry = [&](const UnitDesc& d, int slot, int e, int& blk, int& bits) {
+  auto entry = [&](const UnitDesc& d, int slot, int e, int& blk, int& bits, bool& virt) {
     const bool pad = e >= d.n_ent;
     const int ee = pad ? d.n_ent - 1 : e;
+    virt = false;
     if (d.dense) {
       blk = ee;
       bits = 3;
     } else {
-      const int32_t v = ent_buf(slot)[ee];
-      blk = static_cast<int>(static_cast<uint32_t>(v) & kEntBlockMask);
-      bits = static_cast<int>(static_cast<uint32_t>(v) >> kEntMaskShift);
+      const uint32_t v = static_cast<uint32_t>(ent_buf(slot)[ee]);
+      virt = kMerged && (v & kEntVirtual) != 0;
+      blk = static_cast<int>(v & kEntBlockMask);
+      bits = static_cast<int>(v >> kEntMaskShift);
     }
     if (pad) bits = 0;
   };
@@ -358,6 +371,32 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
               __syncwarp();
             }
             d.n_ent = pos;
+            if (kMerged) {
+              // Every video block the lists skip enters as one summary key:
+              // append the chunks of 64 summary keys, masked per row half.
+              const int nvc = (g.nvk + kBlock - 1) / kBlock;
+              unsigned long long* vm = vmask(slot);
+              for (int c = lane; c < nvc; c += 32) {
+                const int nb = min(kBlock, g.nvk - kBlock * c);
+                const unsigned long long all = (nb == kBlock) ? ~0ull : ((1ull << nb) - 1ull);
+                vm[2 * c] = all;
+                vm[2 * c + 1] = (d.iB >= 0) ? all : 0ull;
+              }
+              __syncwarp();
+              for (int m = lane; m < pos; m += 32) {
+                const uint32_t v = static_cast<uint32_t>(mg[m]);
+                const int blk = static_cast<int>(v & kEntBlockMask);
+                if (blk >= g.nvk) continue;
+                const unsigned long long bit = 1ull << (blk % kBlock);
+                if (v & (1u << kEntMaskShift)) atomicAnd(&vm[2 * (blk / kBlock)], ~bit);
+                if (v & (2u << kEntMaskShift)) atomicAnd(&vm[2 * (blk / kBlock) + 1], ~bit);
+              }
+              const uint32_t hb = (d.iB >= 0) ? 3u : 1u;
+              for (int c = lane; c < nvc; c += 32)
+                mg[pos + c] = static_cast<int32_t>(static_cast<uint32_t>(c) | kEntVirtual | (hb << kEntMaskShift));
+              __syncwarp();
+              d.n_ent = pos + nvc;
+            }
           }
         }
       }
@@ -377,6 +416,10 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
+      if (kMerged) {
+        tma_prefetch_desc(&tm_ak);
+        tma_prefetch_desc(&tm_av);
+      }
       int seq = 0;
       bool ok = true;
       for (int k = 0; ok; ++k) {
@@ -393,7 +436,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         tma_load_2d(sQ + 16384, &tm_q, bar(BAR_QFULL + slot), xq + 64, d.row0);
         // Load order (the MMA thread consumes in the same order): K0, K1,
         // then per step j: V_j, K_{j+2}.
-        auto load = [&](const CUtensorMap* map, int step) -> bool {
+        // kind 0: K (or summary keys), kind 1: V (or summary values)
+        auto load = [&](int kind, int step) -> bool {
           const int s = seq % kSlots;
           const uint32_t par = ((seq / kSlots) & 1) ^ 1;
           if (!mbar_wait(bar(BAR_EMPTY + s), par, kWaitLimitNs)) return false;
@@ -402,18 +446,28 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             int blk, bits;
-            entry(d, slot, 2 * step + hh, blk, bits);
-            tma_load_2d(dst + hh * 8192, map, bar(BAR_FULL + s), xq, blk * kBlock);
-            tma_load_2d(dst + 16384 + hh * 8192, map, bar(BAR_FULL + s), xq + 64, blk * kBlock);
+            bool virt;
+            entry(d, slot, 2 * step + hh, blk, bits, virt);
+            if (!kMerged || !virt) {
+              const CUtensorMap* map = kind == 0 ? &tm_k : &tm_v;
+              tma_load_2d(dst + hh * 8192, map, bar(BAR_FULL + s), xq, blk * kBlock);
+              tma_load_2d(dst + 16384 + hh * 8192, map, bar(BAR_FULL + s), xq + 64, blk * kBlock);
+            } else {
+              // summaries are [H * nblk rows, 128 columns]; K/V [T rows, H * 128]
+              const CUtensorMap* map = kind == 0 ? &tm_ak : &tm_av;
+              const int y0 = d.h * g.nblk + blk * kBlock;
+              tma_load_2d(dst + hh * 8192, map, bar(BAR_FULL + s), 0, y0);
+              tma_load_2d(dst + 16384 + hh * 8192, map, bar(BAR_FULL + s), 64, y0);
+            }
           }
           ++seq;
           return true;
         };
-        ok = load(&tm_k, 0);
-        if (ok && n > 1) ok = load(&tm_k, 1);
+        ok = load(0, 0);
+        if (ok && n > 1) ok = load(0, 1);
         for (int j = 0; j < n && ok; ++j) {
-          ok = load(&tm_v, j);
-          if (ok && j + 2 < n) ok = load(&tm_k, j + 2);
+          ok = load(1, j);
+          if (ok && j + 2 < n) ok = load(0, j + 2);
           if (*s_abort) ok = false;
         }
         if (ok) mbar_arrive(bar(BAR_UEMPTY + slot));
@@ -562,16 +616,31 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // takes the row maximum over both halves, pass 2 reloads each half
         // from tensor memory and turns it into P (keeps 64 values live).
         int blk[2], bits[2];
-        entry(d, slot, 2 * j, blk[0], bits[0]);
-        entry(d, slot, 2 * j + 1, blk[1], bits[1]);
+        bool virt[2];
+        entry(d, slot, 2 * j, blk[0], bits[0], virt[0]);
+        entry(d, slot, 2 * j + 1, blk[1], bits[1], virt[1]);
         bool row_ok[2], fast[2], add_bias[2];
         int nvalid[2];
+        // General path of a half: the additive logits (log2 units) and the
+        // keys that count.  Summary keys (merged mode) take the log-mass and
+        // count only for the video blocks this row half's list skips.
+        auto bias_of = [&](int hh) -> const float4* {
+          if constexpr (kMerged)
+            if (virt[hh])
+              return reinterpret_cast<const float4*>(a.lm2 + static_cast<size_t>(d.h) * a.nblkp +
+                                                     static_cast<size_t>(blk[hh]) * kBlock);
+          return reinterpret_cast<const float4*>(a.b2 + static_cast<size_t>(blk[hh]) * kBlock);
+        };
+        auto keep_of = [&](int hh) -> unsigned long long {
+          if constexpr (kMerged) return virt[hh] ? vmask(slot)[2 * blk[hh] + half] : ~0ull;
+          return ~0ull;
+        };
         float mx = -INFINITY;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           row_ok[hh] = (bits[hh] >> half) & 1;  // uniform across the warp
-          nvalid[hh] = min(kBlock, g.T - blk[hh] * kBlock);
-          add_bias[hh] = (a.b2 != nullptr) && blk[hh] >= g.nvk;
+          nvalid[hh] = virt[hh] ? kBlock : min(kBlock, g.T - blk[hh] * kBlock);
+          add_bias[hh] = virt[hh] || ((a.b2 != nullptr) && blk[hh] >= g.nvk);
           fast[hh] = row_ok[hh] && nvalid[hh] == kBlock && !add_bias[hh];
           if (!row_ok[hh]) continue;
           uint32_t sh[64];
@@ -584,7 +653,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           if (fast[hh]) {
             mx = fmaxf(mx, max64(sh) * sl2);
           } else {
-            const float4* bb = reinterpret_cast<const float4*>(a.b2 + static_cast<size_t>(blk[hh]) * kBlock);
+            const float4* bb = bias_of(hh);
+            const unsigned long long km = keep_of(hh);
 #pragma unroll
             for (int q4 = 0; q4 < 16; ++q4) {
               const float4 bv = add_bias[hh] ? __ldg(bb + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -592,9 +662,10 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int kx = 4 * q4 + e;
-                const float bk = (kx < nvalid[hh]) ? bq[e] : 0.f;
+                const bool valid = kx < nvalid[hh] && (!kMerged || ((km >> kx) & 1ull));
+                const float bk = valid ? bq[e] : 0.f;
                 const float x = fmaf(__uint_as_float(sh[kx]), sl2, bk);
-                if (kx < nvalid[hh]) mx = fmaxf(mx, x);
+                if (valid) mx = fmaxf(mx, x);
               }
             }
           }
@@ -646,7 +717,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 p[kx / 2] = pack_bf16x2(e0, e1);
               }
             } else {
-              const float4* bb = reinterpret_cast<const float4*>(a.b2 + static_cast<size_t>(blk[hh]) * kBlock);
+              const float4* bb = bias_of(hh);
+              const unsigned long long km = keep_of(hh);
 #pragma unroll
               for (int q4 = 0; q4 < 16; ++q4) {
                 const float4 bv = add_bias[hh] ? __ldg(bb + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -655,9 +727,10 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                   const int kx = 4 * q4 + t;
-                  const float bk = (kx < nvalid[hh]) ? bq[t] : 0.f;
+                  const bool valid = kx < nvalid[hh] && (!kMerged || ((km >> kx) & 1ull));
+                  const float bk = valid ? bq[t] : 0.f;
                   const float x = fmaf(__uint_as_float(sh[kx]), sl2, bk - msub);
-                  e[t] = (kx < nvalid[hh]) ? ex2_approx(x) : 0.f;
+                  e[t] = valid ? ex2_approx(x) : 0.f;
                 }
                 acc[(2 * q4) & 3] = fadd2(acc[(2 * q4) & 3], f2(e[0], e[1]));
                 acc[(2 * q4 + 1) & 3] = fadd2(acc[(2 * q4 + 1) & 3], f2(e[2], e[3]));
@@ -818,25 +891,28 @@ cudaError_t launch_bias_prep(const float* bias, float* b2, int32_t* status, cons
 }
 
 cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                             const AttnArgs& a, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             const CUtensorMap& tak, const CUtensorMap& tav, const AttnArgs& a,
+                             cudaStream_t s) {
+  auto* kern = a.merged ? attention_kernel<true> : attention_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   // The register split redistributes the block's launch allocation; a build
   // that allocated fewer registers per thread would make setmaxnreg.inc wait
   // forever, so refuse to launch it.
-  static int regs = -1;
-  if (regs < 0) {
+  static int regs[2] = {-1, -1};
+  int& rg = regs[a.merged ? 1 : 0];
+  if (rg < 0) {
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, attention_kernel);
+    e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
-    regs = fa.numRegs;
+    rg = fa.numRegs;
   }
-  if (regs * kThreads < static_cast<int>(128 * kRegsControl + 256 * kRegsSoftmax)) return cudaErrorInvalidConfiguration;
+  if (rg * kThreads < static_cast<int>(128 * kRegsControl + 256 * kRegsSoftmax)) return cudaErrorInvalidConfiguration;
   const int units = a.g.H * (a.n_dense + a.n_pairs);
   if (units == 0) return cudaSuccess;
   const int grid = units < sm_count() ? units : sm_count();
-  attention_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, a);
+  kern<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, tak, tav, a);
   return cudaGetLastError();
 }
 

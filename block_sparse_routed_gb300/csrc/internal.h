@@ -51,6 +51,10 @@ struct AttnArgs {
   int n_dense;         // dense 128-row tiles per head
   int n_pairs;         // sparse query-block pairs per head
   float scale_log2;    // log2(e) / sqrt(128)
+  // merged (Spark) mode: skipped video blocks enter as summary keys
+  int merged;
+  const float* lm2;    // log-mass in log2 units [H, nblkp]
+  int nblkp;           // row stride of lm2 (a multiple of 64)
 };
 
 struct ReweightArgs {
@@ -69,8 +73,14 @@ cudaError_t launch_route_topk(const PlanArgs& a, cudaStream_t s);
 cudaError_t launch_bias_prep(const float* bias, float* b2, int32_t* status, const Geometry& g,
                              cudaStream_t s);
 cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                             const AttnArgs& a, cudaStream_t s);
+                             const CUtensorMap& tak, const CUtensorMap& tav, const AttnArgs& a,
+                             cudaStream_t s);
 cudaError_t launch_spark_reweight(const ReweightArgs& r, cudaStream_t s);
+int anchor_chunks(int Nv);
+cudaError_t launch_video_query_mean(const uint16_t* q, float* partial, uint16_t* anchor, int H, int Nv,
+                                    cudaStream_t s);
+cudaError_t launch_logmass_log2(const float* lm, float* lm2, int H, int nblk, int nvk, int nblkp,
+                                cudaStream_t s);
 size_t route_topk_smem_bytes(const Geometry& g);
 size_t attention_smem_bytes();
 

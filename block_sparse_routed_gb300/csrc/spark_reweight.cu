@@ -176,3 +176,81 @@ cudaError_t launch_spark_reweight(const ReweightArgs& r, cudaStream_t s) {
 }
 
 }  // namespace sa
+
+// ---------------------------------------------------------------- anchors
+// One global representative per head: the mean of the target-video query
+// rows t < Nv, stored as BF16 ("Sol-Attn and Spark for MiniMax-H3", section
+// "Spark inference integration").  Deterministic two-level sum: partial sums
+// over row chunks in a fixed order, then the chunks in order.
+namespace sa {
+namespace {
+
+constexpr int kAnchorRows = 1024;  // rows per partial sum
+
+// grid (chunk, head); thread (slice s = tid % 16, group r = tid / 16) sums
+// dimensions 8s..8s+7 over rows r, r+16, ... of the chunk.
+__global__ void __launch_bounds__(256) anchor_partial_kernel(const uint16_t* __restrict__ q, float* partial,
+                                                             int H, int Nv) {
+  const int c = blockIdx.x, h = blockIdx.y;
+  const int s = threadIdx.x % 16, r = threadIdx.x / 16;
+  const int t0 = c * kAnchorRows, t1 = min(Nv, t0 + kAnchorRows);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int t = t0 + r; t < t1; t += 16) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(q + (static_cast<size_t>(t) * H + h) * kHeadDim) + s);
+    const uint32_t x[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] += __uint_as_float(x[i] << 16);
+      acc[2 * i + 1] += __uint_as_float(x[i] & 0xFFFF0000u);
+    }
+  }
+  __shared__ float red[16][128];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) red[r][8 * s + i] = acc[i];
+  __syncthreads();
+  if (threadIdx.x < kHeadDim) {
+    float sum = 0.f;
+    for (int g = 0; g < 16; ++g) sum += red[g][threadIdx.x];
+    partial[(static_cast<size_t>(h) * gridDim.x + c) * kHeadDim + threadIdx.x] = sum;
+  }
+}
+
+__global__ void anchor_final_kernel(const float* partial, uint16_t* anchor, int nch, int Nv) {
+  const int h = blockIdx.x, d = threadIdx.x;
+  float sum = 0.f;
+  for (int c = 0; c < nch; ++c) sum += partial[(static_cast<size_t>(h) * nch + c) * kHeadDim + d];
+  const float mean = sum / static_cast<float>(Nv);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(0.f), "f"(mean));
+  anchor[static_cast<size_t>(h) * kHeadDim + d] = static_cast<uint16_t>(r & 0xFFFFu);
+}
+
+// log-mass in log2 units, rows padded to `nblkp` with zeros (masked keys)
+__global__ void logmass_log2_kernel(const float* lm, float* lm2, int nblk, int nvk, int nblkp) {
+  const int h = blockIdx.y;
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= nblkp) return;
+  lm2[static_cast<size_t>(h) * nblkp + j] = (j < nvk) ? lm[static_cast<size_t>(h) * nblk + j] * kLog2e : 0.f;
+}
+
+}  // namespace
+
+int anchor_chunks(int Nv) { return (Nv + kAnchorRows - 1) / kAnchorRows; }
+
+cudaError_t launch_video_query_mean(const uint16_t* q, float* partial, uint16_t* anchor, int H, int Nv,
+                                    cudaStream_t s) {
+  const int nch = anchor_chunks(Nv);
+  anchor_partial_kernel<<<dim3(nch, H), 256, 0, s>>>(q, partial, H, Nv);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  anchor_final_kernel<<<H, kHeadDim, 0, s>>>(partial, anchor, nch, Nv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_logmass_log2(const float* lm, float* lm2, int H, int nblk, int nvk, int nblkp,
+                                cudaStream_t s) {
+  logmass_log2_kernel<<<dim3((nblkp + 127) / 128, H), 128, 0, s>>>(lm, lm2, nblk, nvk, nblkp);
+  return cudaGetLastError();
+}
+
+}  // namespace sa

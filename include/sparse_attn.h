@@ -204,6 +204,33 @@ sa_status sparse_attn_spark_reweight(const sa_reweight_params* p, const void* a,
                                      cudaStream_t stream);
 
 /*
+ * Spark's merged attention ("Sol-Attn and Spark for MiniMax-H3", section
+ * "Spark inference integration": one global representative per head formed
+ * by averaging all target-video queries, stored as BF16; global-anchor K/V
+ * and log-mass summaries merged with exact attention).  Same arguments,
+ * lists and exact part as sparse_attn_fwd; in addition, per head, the
+ * anchor a = BF16(mean of q rows t < video_tokens) is formed, its summaries
+ * of every key block are computed as by sparse_attn_spark_reweight (P = 1),
+ * and every video key block j < nvk that a sparse query block's list skips
+ * enters that block's softmax as one extra key: ak[h, j] with logit
+ * q . ak[h, j] / sqrt(128) + lm[h, j] and value av[h, j].  Dense rows are
+ * exact over all keys as in sparse_attn_fwd.  The source pages have no
+ * separate name for this call.
+ *   ws  workspace of at least sparse_attn_spark_ws_bytes(p) bytes, 256-byte
+ *       aligned.  Layout after the 256-byte status area (each part 256-byte
+ *       aligned): key bias in log2 units float32 [T]; anchors BF16 [H, 128];
+ *       anchor partial sums float32 [H, ceil(video_tokens / 1024), 128];
+ *       ak, av BF16 [H, nblk, 128]; lm float32 [H, nblk]; lm in log2 units
+ *       float32 [H, 64 ceil(nvk / 64)].
+ * Errors: as sparse_attn_fwd (with this workspace size); SA_EUNSUPPORTED
+ * also when H * nblk * 128 reaches 2^31.
+ */
+sa_status sparse_attn_spark_ws_bytes(const sa_params* p, uint64_t* out);
+sa_status sparse_attn_spark_fwd(const sa_params* p, const void* q, const void* k, const void* v,
+                                const float* key_bias, const int32_t* idx, const int32_t* cnt,
+                                void* o, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * Reads the device status word of `ws` (written by the last plan or fwd
  * enqueued with it).  Synchronises `stream`.  SA_ECUDA if the copy fails.
  */
