@@ -12,6 +12,7 @@ row, kept key) pair, summed over heads, divided by the step time.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
     python bench.py --op reweight      # Spark virtual summaries instead
+    python bench.py --op spark         # Spark merged attention (plan + merged fwd)
 
 ``--op reweight`` measures the second operation of the library, the Spark
 virtual summaries (sparse_attn_spark_reweight) over the same H3-shaped K/V
@@ -569,6 +570,88 @@ def run_reweight(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_spark(args, rank, world, local_rank):
+    """Spark's merged attention on the H3 workload: plan + merged forward
+    (anchor, summaries, exact lists plus one summary key per skipped video
+    block).  Reports the step time; the TFLOP/s figure counts the same kept
+    exact work as the headline plus 4 x 128 FLOP per (row, summary key)."""
+    import torch
+
+    import block_sparse_routed_gb300 as bsr
+    from block_sparse_routed_gb300 import _native
+    from workloads import make_workload
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    bsr.load_library()
+    arrays, prm = make_workload(WORKLOAD)
+    T, H, Nv = prm["T"], prm["H"], prm["video_tokens"]
+    P = bsr.Params(T=T, H=H, video_tokens=Nv, topk_ratio=prm["topk_ratio"], radius=prm["radius"],
+                   tail_mode=prm["tail_mode"])
+    sz = bsr.sparse_attn_query(P)
+    dv = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).reshape(1, T, H, 128).to(dev)
+    q, k, v = dv(arrays["q"]), dv(arrays["k"]), dv(arrays["v"])
+    idx = torch.empty((1, H, sz.nq, sz.maxl), dtype=torch.int32, device=dev)
+    cnt = torch.empty((1, H, sz.nq), dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    ws_plan = torch.empty(sz.plan_ws_bytes, dtype=torch.uint8, device=dev)
+    ws = torch.empty(_native.sparse_attn_spark_ws_bytes(P.to_c()), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        bsr.sparse_attn_plan(P, q, k, idx=idx, cnt=cnt, ws=ws_plan, stream=stream)
+        bsr.sparse_attn_spark_fwd(P, q, k, v, idx, cnt, o=o, ws=ws, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    if bsr.sparse_attn_last_device_status(ws, stream) != 0:
+        raise RuntimeError("device status error after warm-up")
+    ic, cc = idx.cpu().numpy().reshape(H, sz.nq, sz.maxl), cnt.cpu().numpy().reshape(H, sz.nq)
+    kept = kept_pairs_from_lists(idx.cpu().numpy(), cnt.cpu().numpy(), T, sz.nvk, sz.nq, Nv,
+                                 sz.dense_row_start) * 4 * 128
+    summary_keys = 0
+    for h in range(H):
+        for i in range(sz.nq):
+            listed = int(np.count_nonzero(ic[h, i, :cc[h, i]] < sz.nvk))
+            rows = min(64, Nv - 64 * i) if i == sz.nvk else 64
+            summary_keys += rows * (sz.nvk - listed)
+    work = kept + summary_keys * 4 * 128
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for s in range(args.steps):
+        ev[s][0].record(stream)
+        bsr.sparse_attn_plan(P, q, k, idx=idx, cnt=cnt, ws=ws_plan, stream=stream)
+        ev[s][1].record(stream)
+        bsr.sparse_attn_spark_fwd(P, q, k, v, idx, cnt, o=o, ws=ws, stream=stream)
+        ev[s][2].record(stream)
+    torch.cuda.synchronize(dev)
+    plan_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    fwd_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    ms = max_over_ranks(plan_ms + fwd_ms, world, dev)
+    if rank != 0:
+        return
+    line = {
+        "metric": "Spark merged attention TFLOP/s (exact lists + one summary key per skipped block), H3",
+        "value": weak_scaling_value(work, ms, world),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "plan_ms": plan_ms,
+        "fwd_ms": fwd_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": dict(workload_config(prm), summary_keys_per_step=summary_keys),
+        "work_tflop_per_step": work / 1e12,
+        "exact_kept_tflop_per_step": kept / 1e12,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -576,7 +659,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["attention", "reweight"], default="attention")
+    ap.add_argument("--op", choices=["attention", "reweight", "spark"], default="attention")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -593,6 +676,8 @@ def main():
     try:
         if args.op == "reweight":
             run_reweight(args, rank, world, local_rank)
+        elif args.op == "spark":
+            run_spark(args, rank, world, local_rank)
         else:
             run_ours(args, rank, world, local_rank)
     finally:

@@ -146,8 +146,8 @@ bool make_map(CUtensorMap* m, const void* ptr, const Geometry& g, uint32_t box_r
 
 // Workspace of the merged (Spark) forward, after the 256-byte status area.
 struct SparkLayout {
-  uint64_t b2, anchor, partial, ak, av, lm, lm2, total;
-  int nch, nblkp;
+  uint64_t b2, anchor, partial, ak, av, lm, lm2, vbias, total;
+  int nch, nblkp, vstride;
 };
 SparkLayout spark_layout(const Geometry& g) {
   SparkLayout L;
@@ -162,6 +162,8 @@ SparkLayout spark_layout(const Geometry& g) {
   L.av = off;      off += align256(H * nblk * kHeadDim * 2);
   L.lm = off;      off += align256(H * nblk * 4);
   L.lm2 = off;     off += align256(H * L.nblkp * 4);
+  L.vstride = 2 * L.nblkp;  // nvc chunks x 2 row halves x 64 keys
+  L.vbias = off;   off += align256(uint64_t(kMaxMergedCtas) * 2 * L.vstride * 4);
   L.total = off;
   return L;
 }
@@ -245,6 +247,8 @@ SA_API sa_status sparse_attn_fwd(const sa_params* p, const void* q, const void* 
   a.merged = 0;
   a.lm2 = nullptr;
   a.nblkp = 0;
+  a.vbias = nullptr;
+  a.vstride = 0;
   // the summary maps are unused without merging
   if (cuda_failed(launch_attention(tq, tk, tv, tk, tv, a, stream))) return SA_ECUDA;
   return SA_OK;
@@ -328,6 +332,8 @@ SA_API sa_status sparse_attn_spark_fwd(const sa_params* p, const void* q, const 
   a.merged = 1;
   a.lm2 = lm2;
   a.nblkp = L.nblkp;
+  a.vbias = reinterpret_cast<float*>(w + L.vbias);
+  a.vstride = L.vstride;
   if (cuda_failed(launch_attention(tq, tk, tv, tak, tav, a, stream))) return SA_ECUDA;
   return SA_OK;
 }

@@ -391,6 +391,17 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (v & (1u << kEntMaskShift)) atomicAnd(&vm[2 * (blk / kBlock)], ~bit);
                 if (v & (2u << kEntMaskShift)) atomicAnd(&vm[2 * (blk / kBlock) + 1], ~bit);
               }
+              __syncwarp();
+              // Additive logits of the summary keys, per row half: the
+              // log-mass where the half's list skips the block, -inf where
+              // it lists it.  Written to this CTA's rows for the slot; the
+              // unit's descriptor barrier publishes them.
+              float* vb = a.vbias + (static_cast<size_t>(blockIdx.x) * 2 + slot) * a.vstride;
+              const float* lmh = a.lm2 + static_cast<size_t>(d.h) * a.nblkp;
+              for (int e = lane; e < nvc * 2 * kBlock; e += 32) {
+                const int c = e / (2 * kBlock), hf = (e / kBlock) & 1, u = e % kBlock;
+                vb[e] = ((vm[2 * c + hf] >> u) & 1ull) ? lmh[kBlock * c + u] : -INFINITY;
+              }
               const uint32_t hb = (d.iB >= 0) ? 3u : 1u;
               for (int c = lane; c < nvc; c += 32)
                 mg[pos + c] = static_cast<int32_t>(static_cast<uint32_t>(c) | kEntVirtual | (hb << kEntMaskShift));
@@ -621,20 +632,18 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         entry(d, slot, 2 * j + 1, blk[1], bits[1], virt[1]);
         bool row_ok[2], fast[2], add_bias[2];
         int nvalid[2];
-        // General path of a half: the additive logits (log2 units) and the
-        // keys that count.  Summary keys (merged mode) take the log-mass and
-        // count only for the video blocks this row half's list skips.
+        // Additive logits (log2 units) of a half on the general path: the
+        // key bias on sinks, or (merged mode) the summary keys' log-mass,
+        // -inf for the blocks this row half's list holds exactly.
         auto bias_of = [&](int hh) -> const float4* {
           if constexpr (kMerged)
             if (virt[hh])
-              return reinterpret_cast<const float4*>(a.lm2 + static_cast<size_t>(d.h) * a.nblkp +
-                                                     static_cast<size_t>(blk[hh]) * kBlock);
+              return reinterpret_cast<const float4*>(
+                  a.vbias + (static_cast<size_t>(blockIdx.x) * 2 + slot) * a.vstride + (2 * blk[hh] + half) * kBlock);
           return reinterpret_cast<const float4*>(a.b2 + static_cast<size_t>(blk[hh]) * kBlock);
         };
-        auto keep_of = [&](int hh) -> unsigned long long {
-          if constexpr (kMerged) return virt[hh] ? vmask(slot)[2 * blk[hh] + half] : ~0ull;
-          return ~0ull;
-        };
+        // summary-key logits are rewritten every other unit: read them past L1
+        auto bias_ld = [&](const float4* p) { return kMerged ? __ldcg(p) : __ldg(p); };
         float mx = -INFINITY;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
@@ -654,15 +663,14 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             mx = fmaxf(mx, max64(sh) * sl2);
           } else {
             const float4* bb = bias_of(hh);
-            const unsigned long long km = keep_of(hh);
 #pragma unroll
             for (int q4 = 0; q4 < 16; ++q4) {
-              const float4 bv = add_bias[hh] ? __ldg(bb + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
+              const float4 bv = add_bias[hh] ? bias_ld(bb + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
               const float bq[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int kx = 4 * q4 + e;
-                const bool valid = kx < nvalid[hh] && (!kMerged || ((km >> kx) & 1ull));
+                const bool valid = kx < nvalid[hh];
                 const float bk = valid ? bq[e] : 0.f;
                 const float x = fmaf(__uint_as_float(sh[kx]), sl2, bk);
                 if (valid) mx = fmaxf(mx, x);
@@ -718,16 +726,15 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
               }
             } else {
               const float4* bb = bias_of(hh);
-              const unsigned long long km = keep_of(hh);
 #pragma unroll
               for (int q4 = 0; q4 < 16; ++q4) {
-                const float4 bv = add_bias[hh] ? __ldg(bb + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 bv = add_bias[hh] ? bias_ld(bb + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
                 const float bq[4] = {bv.x, bv.y, bv.z, bv.w};
                 float e[4];
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                   const int kx = 4 * q4 + t;
-                  const bool valid = kx < nvalid[hh] && (!kMerged || ((km >> kx) & 1ull));
+                  const bool valid = kx < nvalid[hh];
                   const float bk = valid ? bq[t] : 0.f;
                   const float x = fmaf(__uint_as_float(sh[kx]), sl2, bk - msub);
                   e[t] = valid ? ex2_approx(x) : 0.f;
@@ -912,6 +919,7 @@ cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const
   const int units = a.g.H * (a.n_dense + a.n_pairs);
   if (units == 0) return cudaSuccess;
   const int grid = units < sm_count() ? units : sm_count();
+  if (a.merged && grid > kMaxMergedCtas) return cudaErrorInvalidConfiguration;
   kern<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, tak, tav, a);
   return cudaGetLastError();
 }

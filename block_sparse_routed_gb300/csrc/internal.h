@@ -55,7 +55,11 @@ struct AttnArgs {
   int merged;
   const float* lm2;    // log-mass in log2 units [H, nblkp]
   int nblkp;           // row stride of lm2 (a multiple of 64)
+  float* vbias;        // per CTA and descriptor slot: summary-key logits [nvc][2][64]
+  int vstride;         // floats per (CTA, slot): nvc * 2 * 64
 };
+
+constexpr int kMaxMergedCtas = 256;  // CTAs a merged launch may use (summary-key logit rows)
 
 struct ReweightArgs {
   const uint16_t* a;   // BF16 anchors [P, H, 128]

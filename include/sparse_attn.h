@@ -221,7 +221,8 @@ sa_status sparse_attn_spark_reweight(const sa_reweight_params* p, const void* a,
  *       aligned): key bias in log2 units float32 [T]; anchors BF16 [H, 128];
  *       anchor partial sums float32 [H, ceil(video_tokens / 1024), 128];
  *       ak, av BF16 [H, nblk, 128]; lm float32 [H, nblk]; lm in log2 units
- *       float32 [H, 64 ceil(nvk / 64)].
+ *       float32 [H, 64 ceil(nvk / 64)]; summary-key logits of each
+ *       attention CTA float32 [256][2][ceil(nvk / 64)][2][64].
  * Errors: as sparse_attn_fwd (with this workspace size); SA_EUNSUPPORTED
  * also when H * nblk * 128 reaches 2^31.
  */
