@@ -642,8 +642,9 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                   a.vbias + (static_cast<size_t>(blockIdx.x) * 2 + slot) * a.vstride + (2 * blk[hh] + half) * kBlock);
           return reinterpret_cast<const float4*>(a.b2 + static_cast<size_t>(blk[hh]) * kBlock);
         };
-        // summary-key logits are rewritten every other unit: read them past L1
-        auto bias_ld = [&](const float4* p) { return kMerged ? __ldcg(p) : __ldg(p); };
+        // Summary-key logits are rewritten every other unit by this CTA:
+        // ordinary (coherent) loads, ordered after the descriptor barrier.
+        auto bias_ld = [&](const float4* p) { return kMerged ? *p : __ldg(p); };
         float mx = -INFINITY;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
