@@ -50,6 +50,7 @@ __all__ = [
     "sparse_attn_query",
     "sparse_attn_status_string",
     "spark_attn",
+    "sparse_attn_fused",
     "spark_reweight",
     "sparse_attn_spark_fwd",
 ]
@@ -280,3 +281,41 @@ def spark_attn(params: Params, q, k, v, key_bias=None, check_status=True, stream
         if st != SA_OK:
             raise SparseAttnError(st, "spark_attn (device)")
     return o
+
+
+def sparse_attn_fused(params: Params, q, k, v, key_bias=None, idx=None, cnt=None, o=None, ws=None,
+                      stream=None):
+    """Routing and attention in one call, the Top-K taken inside the
+    attention kernel.  Returns (o, idx, cnt); the lists equal
+    sparse_attn_plan's.  The device status is read with
+    ``sparse_attn_last_device_status(ws)`` when ``ws`` is given."""
+    torch = _torch()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_qkv(t, n, params)
+    cp = params.to_c()
+    sz = _native.sparse_attn_query(cp)
+    dev = q.device
+    if key_bias is not None:
+        if (key_bias.dtype != torch.float32 or not key_bias.is_contiguous()
+                or key_bias.numel() != params.B * params.T or not key_bias.is_cuda):
+            raise ValueError("key_bias must be a contiguous CUDA float32 tensor with B*T elements")
+    if idx is None:
+        idx = torch.empty((1, params.H, sz.nq, sz.maxl), dtype=torch.int32, device=dev)
+    if cnt is None:
+        cnt = torch.empty((1, params.H, sz.nq), dtype=torch.int32, device=dev)
+    if o is None:
+        o = torch.empty_like(q)
+    _check_qkv(o, "o", params)
+    for t, n, want in ((idx, "idx", params.H * sz.nq * sz.maxl), (cnt, "cnt", params.H * sz.nq)):
+        if t.dtype != torch.int32 or not t.is_contiguous() or t.numel() != want:
+            raise ValueError(f"{n}: int32 contiguous tensor with {want} elements required")
+    nbytes = _native.sparse_attn_fused_ws_bytes(cp)
+    if ws is None:
+        ws = _workspace(nbytes, dev)
+    st = _native.sparse_attn_fused(cp, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                   key_bias.data_ptr() if key_bias is not None else 0,
+                                   idx.data_ptr(), cnt.data_ptr(), o.data_ptr(), ws.data_ptr(),
+                                   ws.numel(), _stream_handle(stream))
+    if st != SA_OK:
+        raise SparseAttnError(st, "sparse_attn_fused")
+    return o, idx, cnt

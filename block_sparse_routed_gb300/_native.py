@@ -32,6 +32,8 @@ ENTRY_POINTS = (
     "sparse_attn_spark_reweight",
     "sparse_attn_spark_ws_bytes",
     "sparse_attn_spark_fwd",
+    "sparse_attn_fused_ws_bytes",
+    "sparse_attn_fused",
     "sparse_attn_last_device_status",
     "sparse_attn_last_cuda_error",
     "sparse_attn_status_string",
@@ -122,6 +124,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sparse_attn_spark_ws_bytes.restype = ctypes.c_int
     lib.sparse_attn_spark_fwd.argtypes = [P(SaParams), vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.sparse_attn_spark_fwd.restype = ctypes.c_int
+    lib.sparse_attn_fused_ws_bytes.argtypes = [P(SaParams), P(ctypes.c_uint64)]
+    lib.sparse_attn_fused_ws_bytes.restype = ctypes.c_int
+    lib.sparse_attn_fused.argtypes = [P(SaParams), vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.sparse_attn_fused.restype = ctypes.c_int
     lib.sparse_attn_status_string.argtypes = [ctypes.c_int]
     lib.sparse_attn_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -182,6 +188,21 @@ def sparse_attn_spark_ws_bytes(params) -> int:
 def sparse_attn_spark_fwd(params, q, k, v, key_bias, idx, cnt, o, ws, ws_bytes, stream) -> int:
     """Raw call of the merged (Spark) forward.  Returns the status."""
     return load_library().sparse_attn_spark_fwd(
+        ctypes.byref(params), q, k, v, key_bias or None, idx, cnt, o, ws, ws_bytes, stream or None
+    )
+
+
+def sparse_attn_fused_ws_bytes(params) -> int:
+    out = ctypes.c_uint64(0)
+    st = load_library().sparse_attn_fused_ws_bytes(ctypes.byref(params), ctypes.byref(out))
+    if st != SA_OK:
+        raise SparseAttnError(st, "sparse_attn_fused_ws_bytes")
+    return int(out.value)
+
+
+def sparse_attn_fused(params, q, k, v, key_bias, idx, cnt, o, ws, ws_bytes, stream) -> int:
+    """Raw call of the fused (in-kernel routing) entry point.  Returns the status."""
+    return load_library().sparse_attn_fused(
         ctypes.byref(params), q, k, v, key_bias or None, idx, cnt, o, ws, ws_bytes, stream or None
     )
 

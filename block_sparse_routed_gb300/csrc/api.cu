@@ -249,7 +249,99 @@ SA_API sa_status sparse_attn_fwd(const sa_params* p, const void* q, const void* 
   a.nblkp = 0;
   a.vbias = nullptr;
   a.vstride = 0;
+  a.fused = 0;
+  a.qc = a.kc = nullptr;
+  a.idx_w = a.cnt_w = nullptr;
   // the summary maps are unused without merging
+  if (cuda_failed(launch_attention(tq, tk, tv, tk, tv, a, stream))) return SA_ECUDA;
+  return SA_OK;
+}
+
+// Workspace of the fused call, after the 256-byte status area: key bias in
+// log2 units [T], Qmean [H, nq, 128], Kmean [H, nvk, 128].
+struct FusedLayout {
+  uint64_t b2, qc, kc, total;
+};
+FusedLayout fused_layout(const Geometry& g) {
+  FusedLayout L;
+  uint64_t off = kStatusBytes;
+  L.b2 = off; off += align256(uint64_t(g.T) * 4);
+  L.qc = off; off += align256(uint64_t(g.H) * g.nq * kHeadDim * 4);
+  L.kc = off; off += align256(uint64_t(g.H) * g.nvk * kHeadDim * 4);
+  L.total = off;
+  return L;
+}
+
+SA_API sa_status sparse_attn_fused_ws_bytes(const sa_params* p, uint64_t* out) {
+  if (out == nullptr) return SA_EINVAL;
+  Geometry g;
+  const sa_status st = derive(p, &g, nullptr);
+  if (st != SA_OK) return st;
+  if (g.nvk > kMaxFusedVideoBlocks) return SA_EUNSUPPORTED;
+  *out = fused_layout(g).total;
+  return SA_OK;
+}
+
+SA_API sa_status sparse_attn_fused(const sa_params* p, const void* q, const void* k, const void* v,
+                                   const float* key_bias, int32_t* idx, int32_t* cnt, void* o, void* ws,
+                                   size_t ws_bytes, cudaStream_t stream) {
+  Geometry g;
+  sa_sizes sz;
+  sa_status st = derive(p, &g, &sz);
+  if (st != SA_OK) return st;
+  if (g.nvk > kMaxFusedVideoBlocks) return SA_EUNSUPPORTED;
+  if (!q || !k || !v || !idx || !cnt || !o || !ws) return SA_EINVAL;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(idx, 4) || !aligned(cnt, 4) || !aligned(ws, 256) ||
+      (key_bias && !aligned(key_bias, 4)))
+    return SA_EINVAL;
+  const FusedLayout L = fused_layout(g);
+  if (ws_bytes < L.total) return SA_EINVAL;
+  st = check_device();
+  if (st != SA_OK) return st;
+
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, q, g, 128) || !make_map(&tk, k, g, 64) || !make_map(&tv, v, g, 64))
+    return SA_ECUDA;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* status = reinterpret_cast<int32_t*>(w);
+  float* b2 = key_bias ? reinterpret_cast<float*>(w + L.b2) : nullptr;
+  if (cuda_failed(cudaMemsetAsync(ws, 0, kStatusBytes, stream))) return SA_ECUDA;
+  // block means (the routing kernel's first half); the route runs in the
+  // attention kernel's scheduler
+  PlanArgs pa;
+  pa.q = static_cast<const uint16_t*>(q);
+  pa.k = static_cast<const uint16_t*>(k);
+  pa.qc = reinterpret_cast<float*>(w + L.qc);
+  pa.kc = reinterpret_cast<float*>(w + L.kc);
+  pa.idx = idx;
+  pa.cnt = cnt;
+  pa.scores = nullptr;
+  pa.g = g;
+  if (cuda_failed(launch_pool(pa, stream))) return SA_ECUDA;
+  if (key_bias && cuda_failed(launch_bias_prep(key_bias, b2, status, g, stream))) return SA_ECUDA;
+
+  AttnArgs a;
+  a.idx = idx;
+  a.cnt = cnt;
+  a.b2 = b2;
+  a.o = static_cast<uint16_t*>(o);
+  a.status = status;
+  a.unit_counter = status + 1;  // inside the status area, cleared above
+  a.g = g;
+  a.n_dense = (g.T - g.r0 + 127) / 128;
+  a.n_pairs = (g.nq + 1) / 2;
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(128.0));
+  a.merged = 0;
+  a.lm2 = nullptr;
+  a.nblkp = 0;
+  a.vbias = nullptr;
+  a.vstride = 0;
+  a.fused = 1;
+  a.qc = pa.qc;
+  a.kc = pa.kc;
+  a.idx_w = idx;
+  a.cnt_w = cnt;
   if (cuda_failed(launch_attention(tq, tk, tv, tk, tv, a, stream))) return SA_ECUDA;
   return SA_OK;
 }
@@ -334,6 +426,9 @@ SA_API sa_status sparse_attn_spark_fwd(const sa_params* p, const void* q, const 
   a.nblkp = L.nblkp;
   a.vbias = reinterpret_cast<float*>(w + L.vbias);
   a.vstride = L.vstride;
+  a.fused = 0;
+  a.qc = a.kc = nullptr;
+  a.idx_w = a.cnt_w = nullptr;
   if (cuda_failed(launch_attention(tq, tk, tv, tak, tav, a, stream))) return SA_ECUDA;
   return SA_OK;
 }

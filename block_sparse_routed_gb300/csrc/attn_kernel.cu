@@ -82,7 +82,8 @@ constexpr uint32_t kOffRing = 2 * kQBytes;                      // kSlots x kSlo
 constexpr uint32_t kOffEnt = kOffRing + kSlots * kSlotBytes;    // 2 x kMaxEnt int32
 constexpr uint32_t kOffScratch = kOffEnt + 2 * 4 * kMaxEnt;     // 2 x kMaxList int32 (merge)
 constexpr uint32_t kOffMask = kOffScratch + 2 * 4 * kMaxList;   // 2 x [kMaxChunks][2] uint64
-constexpr uint32_t kOffXchg = kOffMask + 2 * 8 * 2 * kMaxChunks; // [3][128] refs + [2][128] sums
+constexpr uint32_t kOffQrow = kOffMask + 2 * 8 * 2 * kMaxChunks; // 2 x 128 float (fused route)
+constexpr uint32_t kOffXchg = kOffQrow + 2 * 4 * kHeadDim;       // [3][128] refs + [2][128] sums
 constexpr uint32_t kOffUnit = kOffXchg + 4 * 5 * 128;           // 2 unit descriptors
 constexpr uint32_t kOffBar = kOffUnit + 64;
 constexpr uint32_t kOffMisc = kOffBar + 512;
@@ -124,6 +125,14 @@ static_assert(sizeof(UnitDesc) * 2 <= 64, "unit area");
 constexpr uint32_t kEntMaskShift = 30;
 constexpr uint32_t kEntVirtual = 1u << 29;          // a chunk of 64 summary keys
 constexpr uint32_t kEntBlockMask = kEntVirtual - 1u;
+
+// Order-preserving map of an FP32 score to an unsigned key; -0 and +0 map to
+// the same key (the routing kernel's convention).
+__device__ __forceinline__ uint32_t order_key_f(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (f == 0.0f) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
 
 __device__ __forceinline__ int lower_bound_s(const int32_t* a, int n, int32_t x) {
   int lo = 0, hi = n;
@@ -225,9 +234,11 @@ __device__ __forceinline__ void decode_unit(const AttnArgs& a, int u, UnitDesc& 
 }
 
 // kMerged: Spark's merged mode (skipped video blocks enter as summary keys).
-// The exact path is a separate instantiation so that its softmax code stays
-// as compact as it can be.
-template <bool kMerged>
+// kFused: the scheduler routes each unit itself (CTA-local Top-K from the
+// block means) instead of reading the plan's lists, and exports the lists.
+// Each mode is its own instantiation so that the exact path's softmax code
+// stays as compact as it can be.
+template <bool kMerged, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
 attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_ak,
@@ -298,6 +309,138 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     return mbar_wait(bar(BAR_UFULL + (k & 1)), (k >> 1) & 1, kWaitLimitNs);
   };
 
+  // Fused route of a sparse unit (scheduler warp): for query blocks iA and
+  // iB, the scores s_j = Qmean . Kmean_j / sqrt(128) summed in FP32 over
+  // d = 0..127 in order (as the routing kernel does), Top-K by the bitwise
+  // boundary search, and the sorted union of forced local blocks, selected
+  // blocks and sinks, written to la / lb and exported to idx / cnt.
+  auto route_pair = [&](const UnitDesc& d, int32_t* la_, int32_t* lb_) -> int2 {
+    float* qs = reinterpret_cast<float*>(base + kOffQrow);
+    const int nrow = d.iB >= 0 ? 2 : 1;
+    for (int e = lane; e < nrow * kHeadDim; e += 32) {
+      const int i = e < kHeadDim ? d.iA : d.iB;
+      qs[e] = a.qc[(static_cast<size_t>(d.h) * g.nq + i) * kHeadDim + (e % kHeadDim)];
+    }
+    __syncwarp();
+    constexpr int kKpl = kMaxFusedVideoBlocks / 32;  // keys per lane
+    uint32_t kr[2][kKpl];
+    const float inv_sqrt_d = 0.08838834764831845f;  // 1/sqrt(128)
+    // All of a lane's keys advance together over d = 0..127 (each sum still
+    // in order of d): 2 x kKpl independent FMA chains instead of two.
+    float acc[2][kKpl];
+#pragma unroll
+    for (int m = 0; m < kKpl; ++m) acc[0][m] = acc[1][m] = 0.f;
+    const float4* kbase = reinterpret_cast<const float4*>(a.kc + static_cast<size_t>(d.h) * g.nvk * kHeadDim);
+#pragma unroll 1
+    for (int d4 = 0; d4 < kHeadDim / 4; ++d4) {
+      const float4 q0 = *reinterpret_cast<const float4*>(qs + 4 * d4);
+      const float4 q1 = *reinterpret_cast<const float4*>(qs + kHeadDim + 4 * d4);
+#pragma unroll
+      for (int m = 0; m < kKpl; ++m) {
+        const int j = lane + 32 * m;
+        if (j < g.nvk) {
+          const float4 kv = __ldg(kbase + static_cast<size_t>(j) * (kHeadDim / 4) + d4);
+          acc[0][m] = fmaf(q0.x, kv.x, acc[0][m]);
+          acc[0][m] = fmaf(q0.y, kv.y, acc[0][m]);
+          acc[0][m] = fmaf(q0.z, kv.z, acc[0][m]);
+          acc[0][m] = fmaf(q0.w, kv.w, acc[0][m]);
+          acc[1][m] = fmaf(q1.x, kv.x, acc[1][m]);
+          acc[1][m] = fmaf(q1.y, kv.y, acc[1][m]);
+          acc[1][m] = fmaf(q1.z, kv.z, acc[1][m]);
+          acc[1][m] = fmaf(q1.w, kv.w, acc[1][m]);
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < kKpl; ++m) {
+      const int j = lane + 32 * m;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int i = r == 0 ? d.iA : d.iB;
+        const int lo = max(0, i - g.R), hi = min(g.nvk - 1, i + g.R);
+        const bool cand = j < g.nvk && (j < lo || j > hi) && (r == 0 || d.iB >= 0);
+        kr[r][m] = cand ? order_key_f(acc[r][m] * inv_sqrt_d) : 0u;
+      }
+    }
+    // largest tau with #{keys >= tau} >= kp, both rows' searches together
+    int kp[2], need[2];
+    bool take_all[2];
+    uint32_t tau[2] = {0u, 0u};
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int i = r == 0 ? d.iA : (d.iB >= 0 ? d.iB : d.iA);
+      const int lo = max(0, i - g.R), hi = min(g.nvk - 1, i + g.R);
+      const int ncand = g.nvk - max(0, hi - lo + 1);
+      kp[r] = min(g.K, ncand);
+      take_all[r] = kp[r] == ncand;
+    }
+#pragma unroll 1
+    for (int bit = 31; bit >= 0; --bit) {
+      unsigned c[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const uint32_t t = tau[r] | (1u << bit);
+        c[r] = 0;
+#pragma unroll
+        for (int m = 0; m < kKpl; ++m) c[r] += (kr[r][m] >= t) ? 1u : 0u;
+      }
+#pragma unroll
+      for (int r = 0; r < 2; ++r) c[r] = __reduce_add_sync(0xFFFFFFFFu, c[r]);
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+        if (static_cast<int>(c[r]) >= kp[r]) tau[r] |= (1u << bit);
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      unsigned c = 0;
+#pragma unroll
+      for (int m = 0; m < kKpl; ++m) c += (kr[r][m] > tau[r]) ? 1u : 0u;
+      need[r] = kp[r] - static_cast<int>(__reduce_add_sync(0xFFFFFFFFu, c));
+    }
+    const unsigned lt = (1u << lane) - 1u;
+    int2 cnt_ab = make_int2(0, 0);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      if (r == 1 && d.iB < 0) break;
+      const int i = r == 0 ? d.iA : d.iB;
+      const int lo = max(0, i - g.R), hi = min(g.nvk - 1, i + g.R);
+      int32_t* out = r == 0 ? la_ : lb_;
+      int32_t* gout = a.idx_w + (static_cast<size_t>(d.h) * g.nq + i) * g.maxl;
+      int pos = 0, eq_seen = 0;
+      auto emit = [&](int j, bool sel, bool eq) {
+        const unsigned eqm = __ballot_sync(0xFFFFFFFFu, eq);
+        if (eq) sel = (eq_seen + __popc(eqm & lt)) < need[r];
+        eq_seen += __popc(eqm);
+        const unsigned sm = __ballot_sync(0xFFFFFFFFu, sel);
+        if (sel) {
+          out[pos + __popc(sm & lt)] = j;
+          gout[pos + __popc(sm & lt)] = j;
+        }
+        pos += __popc(sm);
+      };
+#pragma unroll
+      for (int m = 0; m < kKpl; ++m) {
+        if (32 * m >= g.nblk) break;
+        const int j = 32 * m + lane;
+        bool sel = false, eq = false;
+        if (j < g.nvk) {
+          if ((j >= lo && j <= hi) || take_all[r]) sel = true;
+          else if (kr[r][m] > tau[r]) sel = true;
+          else if (kr[r][m] == tau[r]) eq = true;
+        } else {
+          sel = j < g.nblk;  // sink block
+        }
+        emit(j, sel, eq);
+      }
+      for (int j0 = 32 * kKpl; j0 < g.nblk; j0 += 32) emit(j0 + lane, j0 + lane < g.nblk, false);
+      for (int q = pos + lane; q < g.maxl; q += 32) gout[q] = -1;
+      if (lane == 0) a.cnt_w[static_cast<size_t>(d.h) * g.nq + i] = pos;
+      (r == 0 ? cnt_ab.x : cnt_ab.y) = pos;
+    }
+    __syncwarp();
+    return cnt_ab;
+  };
+
   if (warp < 4) {
     setmaxnreg_dec<kRegsControl>();
   }
@@ -324,15 +467,24 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       } else {
         decode_unit(a, u, d);
         if (!d.dense) {
-          const int nA = a.cnt[static_cast<size_t>(d.h) * g.nq + d.iA];
-          const int nB = (d.iB >= 0) ? a.cnt[static_cast<size_t>(d.h) * g.nq + d.iB] : 0;
+          int nA, nB;
+          if constexpr (kFused) {
+            const int2 n = route_pair(d, la, lb);  // lists straight into la / lb
+            nA = n.x;
+            nB = n.y;
+          } else {
+            nA = a.cnt[static_cast<size_t>(d.h) * g.nq + d.iA];
+            nB = (d.iB >= 0) ? a.cnt[static_cast<size_t>(d.h) * g.nq + d.iB] : 0;
+          }
           bad = nA < 1 || nA > g.maxl || nB < 0 || nB > g.maxl;
           if (!bad) {
-            const int32_t* ga = a.idx + (static_cast<size_t>(d.h) * g.nq + d.iA) * g.maxl;
-            for (int k2 = lane; k2 < nA; k2 += 32) la[k2] = ga[k2];
-            if (d.iB >= 0) {
-              const int32_t* gb = a.idx + (static_cast<size_t>(d.h) * g.nq + d.iB) * g.maxl;
-              for (int k2 = lane; k2 < nB; k2 += 32) lb[k2] = gb[k2];
+            if constexpr (!kFused) {
+              const int32_t* ga = a.idx + (static_cast<size_t>(d.h) * g.nq + d.iA) * g.maxl;
+              for (int k2 = lane; k2 < nA; k2 += 32) la[k2] = ga[k2];
+              if (d.iB >= 0) {
+                const int32_t* gb = a.idx + (static_cast<size_t>(d.h) * g.nq + d.iB) * g.maxl;
+                for (int k2 = lane; k2 < nB; k2 += 32) lb[k2] = gb[k2];
+              }
             }
             __syncwarp();
             for (int k2 = lane; k2 < nA; k2 += 32)
@@ -901,15 +1053,16 @@ cudaError_t launch_bias_prep(const float* bias, float* b2, int32_t* status, cons
 cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                              const CUtensorMap& tak, const CUtensorMap& tav, const AttnArgs& a,
                              cudaStream_t s) {
-  auto* kern = a.merged ? attention_kernel<true> : attention_kernel<false>;
+  auto* kern = a.merged ? attention_kernel<true, false>
+                        : (a.fused ? attention_kernel<false, true> : attention_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   // The register split redistributes the block's launch allocation; a build
   // that allocated fewer registers per thread would make setmaxnreg.inc wait
   // forever, so refuse to launch it.
-  static int regs[2] = {-1, -1};
-  int& rg = regs[a.merged ? 1 : 0];
+  static int regs[3] = {-1, -1, -1};
+  int& rg = regs[a.merged ? 1 : (a.fused ? 2 : 0)];
   if (rg < 0) {
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, kern);

@@ -57,7 +57,16 @@ struct AttnArgs {
   int nblkp;           // row stride of lm2 (a multiple of 64)
   float* vbias;        // per CTA and descriptor slot: summary-key logits [nvc][2][64]
   int vstride;         // floats per (CTA, slot): nvc * 2 * 64
+  // fused mode: the kernel routes each unit from the block means and
+  // exports the lists to idx_w / cnt_w (then read back as idx / cnt)
+  int fused;
+  const float* qc;     // [H, nq, 128]
+  const float* kc;     // [H, nvk, 128]
+  int32_t* idx_w;
+  int32_t* cnt_w;
 };
+
+constexpr int kMaxFusedVideoBlocks = 256;  // video key blocks a fused route supports
 
 constexpr int kMaxMergedCtas = 256;  // CTAs a merged launch may use (summary-key logit rows)
 

@@ -232,6 +232,29 @@ sa_status sparse_attn_spark_fwd(const sa_params* p, const void* q, const void* k
                                 void* o, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * Routing and attention in one call, with the Top-K taken inside the
+ * attention kernel ("Sol-Attn and Spark for MiniMax-H3", section "Spark
+ * inference integration": CTA-local fused Top-K routing, which removes the
+ * external route pass).  Computes exactly what sparse_attn_plan followed by
+ * sparse_attn_fwd computes, with the same FP32 scores and selection rule:
+ * block means first, then each attention work unit scores its query blocks
+ * against every video key block's mean, selects, and walks the lists it
+ * made.  The lists are exported to idx / cnt (the layout of
+ * sparse_attn_plan's outputs; here outputs of this call).
+ *   ws  workspace of at least sparse_attn_fused_ws_bytes(p) bytes, 256-byte
+ *       aligned: 256-byte status area, key bias in log2 units float32 [T],
+ *       Qmean float32 [H, nq, 128], Kmean float32 [H, nvk, 128] (each part
+ *       256-byte aligned).
+ * Errors: as sparse_attn_fwd (with this workspace size); SA_EUNSUPPORTED
+ * also when nvk > 256 (rows of at most 256 video blocks are routed in one
+ * warp's registers).
+ */
+sa_status sparse_attn_fused_ws_bytes(const sa_params* p, uint64_t* out);
+sa_status sparse_attn_fused(const sa_params* p, const void* q, const void* k, const void* v,
+                            const float* key_bias, int32_t* idx, int32_t* cnt, void* o, void* ws,
+                            size_t ws_bytes, cudaStream_t stream);
+
+/*
  * Reads the device status word of `ws` (written by the last plan or fwd
  * enqueued with it).  Synchronises `stream`.  SA_ECUDA if the copy fails.
  */
