@@ -37,3 +37,4 @@ from .spark import (  # noqa: F401
     spark_reweight,
     video_query_anchor,
 )
+from .reblock import reblock_bytes, spark_reblock  # noqa: F401
