@@ -13,6 +13,7 @@ row, kept key) pair, summed over heads, divided by the step time.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
     python bench.py --op reweight      # Spark virtual summaries instead
     python bench.py --op spark         # Spark merged attention (plan + merged fwd)
+    python bench.py --op reblock       # Spark token reblocking (landmark tree) of the H3 keys
 
 ``--op reweight`` measures the second operation of the library, the Spark
 virtual summaries (sparse_attn_spark_reweight) over the same H3-shaped K/V
@@ -471,6 +472,148 @@ def _reweight_worker(args):
     return time.perf_counter() - t0
 
 
+def _reblock_worker(args):
+    x, fanout = args
+    from oracle import reblock as R
+
+    t0 = time.perf_counter()
+    R.reblock_head(x, fanout)
+    return time.perf_counter() - t0
+
+
+def reblock_bytes(T, H):
+    """Samples read once (BF16) plus the permutation and its inverse (int32)."""
+    return T * H * 256 + 2 * T * H * 4
+
+
+def reblock_depth(m, fanout):
+    if m <= 1:
+        return 0
+    c = 1
+    while c * 2 <= min(fanout, m):
+        c *= 2
+    lo = reblock_depth(m // c, fanout)
+    hi = reblock_depth(m // c + 1, fanout) if m % c else lo
+    return 1 + max(lo, hi)
+
+
+def run_reblock(args, rank, world, local_rank):
+    """Spark token reblocking of the H3 keys: algorithmic HBM bytes per second."""
+    import torch
+
+    import block_sparse_routed_gb300 as bsr
+    from workloads import make_workload
+
+    arrays, prm = make_workload(WORKLOAD)
+    T, H = prm["T"], prm["H"]
+    fanout = 8
+    pool = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        pool = _oracle_pool(host_cores())
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    bsr.load_library()
+    hx = torch.from_numpy(np.ascontiguousarray(arrays["k"]).view(np.int16)).view(torch.bfloat16).reshape(T, H, 128).pin_memory()
+    x = hx.to(dev)
+    perm = torch.empty((H, T), dtype=torch.int32, device=dev)
+    inv = torch.empty_like(perm)
+    from block_sparse_routed_gb300 import _native
+
+    rp = _native.SaReblockParams(_native.SA_ABI_VERSION, T, H, 128, fanout, 32, x.stride(0), x.stride(1))
+    ws = torch.empty(max(_native.sparse_attn_reblock_ws_bytes(rp), 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        bsr.spark_reblock(x, fanout=fanout, perm=perm, inv=inv, ws=ws, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    nbytes = reblock_bytes(T, H)
+    clocks = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for e0, e1 in ev:
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    per = [e0.elapsed_time(e1) for e0, e1 in ev]
+    ms = max_over_ranks(sum(per) / len(per), world, dev)
+    value = world * nbytes / (ms * 1e-3) / 1e9
+
+    hperm = torch.empty((H, T), dtype=torch.int32).pin_memory()
+    hinv = torch.empty_like(hperm).pin_memory()
+
+    def e2e_step():
+        x.copy_(hx, non_blocking=True)
+        step()
+        hperm.copy_(perm, non_blocking=True)
+        hinv.copy_(inv, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    if rank != 0:
+        return
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks["hbm_gbs"])
+    cpu = None
+    if pool is not None:
+        try:
+            hs = list(range(min(H, host_cores())))
+            tasks = [(np.ascontiguousarray(arrays["k"][:, h, :]), fanout) for h in hs]
+            t0 = time.perf_counter()
+            pool.map(_reblock_worker, tasks, chunksize=1)
+            secs = time.perf_counter() - t0
+            cpu = {"value": reblock_bytes(T, len(hs)) / secs / 1e9, "unit": "GB/s", "cores": host_cores(),
+                   "kind": "oracle", "seconds": secs,
+                   "sample": f"{len(hs)} of {H} heads, all tokens, one head per task"}
+        finally:
+            pool.close()
+            pool.join()
+    depth = reblock_depth(T // 64, fanout)
+    line = {
+        "metric": "spark_reblock HBM GB/s (landmark-tree token reblocking of the H3 keys)",
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp32",
+        "data": "synthetic",
+        "config": {"workload": "Spark reblocking of the H3 keys (9505 tokens x 56 heads, 128 dims), "
+                               "fanout 8, 32 landmarks", "T": T, "H": H, "fanout": fanout, "landmarks": 32,
+                   "levels": depth, "l2": "samples 136 MB > 126 MB L2, no flush"},
+        "roofline": {"bound": "hbm", "achieved": value, "peak": peak, "unit": "GB/s", "frac": value / peak,
+                     "traffic": None, "kernel": f"whole call ({depth + 2} launches)",
+                     "peak_kind": f"{peak_kind} copy bandwidth"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": T * H * 256, "d2h_bytes_per_step": 2 * T * H * 4, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * (depth + 2),
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def reweight_bytes(P, T, H):
     nblk = (T + 63) // 64
     return 2 * T * H * 256 + P * H * 256 + P * H * nblk * (2 * 256 + 4)
@@ -689,7 +832,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["attention", "reweight", "spark"], default="attention")
+    ap.add_argument("--op", choices=["attention", "reweight", "spark", "reblock"], default="attention")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -708,6 +851,8 @@ def main():
             run_reweight(args, rank, world, local_rank)
         elif args.op == "spark":
             run_spark(args, rank, world, local_rank)
+        elif args.op == "reblock":
+            run_reblock(args, rank, world, local_rank)
         else:
             run_ours(args, rank, world, local_rank)
     finally:

@@ -14,6 +14,8 @@ Two calls, backed by hand-written CUDA kernels in a C-ABI library:
 * ``sparse_attn_spark_fwd`` / ``spark_attn``: Spark's merged attention: the
   exact lists plus one summary key per skipped video block, from a per-head
   anchor (the mean of the target-video queries).
+* ``spark_reblock``: Spark's token reblocking, a per-head permutation of the
+  tokens into 64-token blocks by a landmark tree, and its inverse.
 
 This module marshals torch tensors to the C entry points of the same names.
 PyTorch provides device memory and streams only; every step runs in the
@@ -32,6 +34,7 @@ from ._native import (  # noqa: F401
     SA_EUNSUPPORTED,
     SA_OK,
     SaParams,
+    SaReblockParams,
     SaReweightParams,
     SaSizes,
     SparseAttnError,
@@ -52,6 +55,7 @@ __all__ = [
     "spark_attn",
     "sparse_attn_fused",
     "spark_reweight",
+    "spark_reblock",
     "sparse_attn_spark_fwd",
 ]
 
@@ -238,6 +242,43 @@ def spark_reweight(a, k, v, ak=None, av=None, lm=None, stream=None):
     if st != SA_OK:
         raise SparseAttnError(st, "sparse_attn_spark_reweight")
     return ak, av, lm
+
+
+def spark_reblock(x, fanout=8, landmarks=32, perm=None, inv=None, ws=None, stream=None):
+    """Spark token reblocking of every head's tokens.
+
+    x: CUDA bfloat16 samples [T, H, 128] or [1, T, H, 128] (any strides that
+    are multiples of 8 elements, innermost dimension contiguous).  Returns
+    perm, inv: int32 [H, T] (CUDA), written by the library's kernels:
+    perm[h, i] is the original token at new position i, the blocks are
+    perm[h, :64 * (T // 64)].view(-1, 64) and the excluded remainder is
+    perm[h, 64 * (T // 64):]; inv[h, perm[h, i]] = i.
+    """
+    torch = _torch()
+    if x.dim() == 4:
+        if x.shape[0] != 1:
+            raise ValueError("batch must be 1")
+        x = x[0]
+    if x.dim() != 3 or x.dtype != torch.bfloat16 or not x.is_cuda or x.shape[2] != 128 or x.stride(2) != 1:
+        raise ValueError("x must be a CUDA bfloat16 [T, H, 128] tensor with a contiguous last dimension")
+    T, H, D = x.shape
+    rp = SaReblockParams(_native.SA_ABI_VERSION, T, H, D, fanout, landmarks, x.stride(0), x.stride(1))
+    need = _native.sparse_attn_reblock_ws_bytes(rp)
+    dev = x.device
+    if perm is None:
+        perm = torch.empty((H, T), dtype=torch.int32, device=dev)
+    if inv is None:
+        inv = torch.empty((H, T), dtype=torch.int32, device=dev)
+    for t, n in ((perm, "perm"), (inv, "inv")):
+        if t.dtype != torch.int32 or not t.is_contiguous() or t.numel() != H * T or not t.is_cuda:
+            raise ValueError(f"{n}: contiguous CUDA int32 tensor with {H * T} elements required")
+    if ws is None:
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    st = _native.sparse_attn_spark_reblock(rp, x.data_ptr(), perm.data_ptr(), inv.data_ptr(), ws.data_ptr(),
+                                           ws.numel(), _stream_handle(stream))
+    if st != SA_OK:
+        raise SparseAttnError(st, "sparse_attn_spark_reblock")
+    return perm, inv
 
 
 def sparse_attn_spark_fwd(params: Params, q, k, v, idx, cnt, key_bias=None, o=None, ws=None,

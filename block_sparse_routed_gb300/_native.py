@@ -34,6 +34,8 @@ ENTRY_POINTS = (
     "sparse_attn_spark_fwd",
     "sparse_attn_fused_ws_bytes",
     "sparse_attn_fused",
+    "sparse_attn_reblock_ws_bytes",
+    "sparse_attn_spark_reblock",
     "sparse_attn_last_device_status",
     "sparse_attn_last_cuda_error",
     "sparse_attn_status_string",
@@ -66,6 +68,19 @@ class SaSizes(ctypes.Structure):
         ("dense_row_start", ctypes.c_int32),
         ("plan_ws_bytes", ctypes.c_uint64),
         ("fwd_ws_bytes", ctypes.c_uint64),
+    ]
+
+
+class SaReblockParams(ctypes.Structure):
+    _fields_ = [
+        ("abi_version", ctypes.c_uint32),
+        ("T", ctypes.c_int32),
+        ("H", ctypes.c_int32),
+        ("D", ctypes.c_int32),
+        ("fanout", ctypes.c_int32),
+        ("landmarks", ctypes.c_int32),
+        ("token_stride", ctypes.c_int64),
+        ("head_stride", ctypes.c_int64),
     ]
 
 
@@ -128,6 +143,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sparse_attn_fused_ws_bytes.restype = ctypes.c_int
     lib.sparse_attn_fused.argtypes = [P(SaParams), vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.sparse_attn_fused.restype = ctypes.c_int
+    lib.sparse_attn_reblock_ws_bytes.argtypes = [P(SaReblockParams), P(ctypes.c_uint64)]
+    lib.sparse_attn_reblock_ws_bytes.restype = ctypes.c_int
+    lib.sparse_attn_spark_reblock.argtypes = [P(SaReblockParams), vp, vp, vp, vp, sz, vp]
+    lib.sparse_attn_spark_reblock.restype = ctypes.c_int
     lib.sparse_attn_status_string.argtypes = [ctypes.c_int]
     lib.sparse_attn_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -205,6 +224,20 @@ def sparse_attn_fused(params, q, k, v, key_bias, idx, cnt, o, ws, ws_bytes, stre
     return load_library().sparse_attn_fused(
         ctypes.byref(params), q, k, v, key_bias or None, idx, cnt, o, ws, ws_bytes, stream or None
     )
+
+
+def sparse_attn_reblock_ws_bytes(params) -> int:
+    out = ctypes.c_uint64(0)
+    st = load_library().sparse_attn_reblock_ws_bytes(ctypes.byref(params), ctypes.byref(out))
+    if st != SA_OK:
+        raise SparseAttnError(st, "sparse_attn_reblock_ws_bytes")
+    return int(out.value)
+
+
+def sparse_attn_spark_reblock(params, x, perm, inv, ws, ws_bytes, stream) -> int:
+    """Raw call of the reblocking entry point.  Returns the status."""
+    return load_library().sparse_attn_spark_reblock(ctypes.byref(params), x, perm, inv, ws, ws_bytes,
+                                                    stream or None)
 
 
 def sparse_attn_last_device_status(ws, stream) -> int:

@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB_NAME = "libsparse_attn.so"
 LIB_PATH = os.path.join(OUT, LIB_NAME)
-SOURCES = ["api.cu", "plan_kernels.cu", "attn_kernel.cu", "plan_static.cu", "spark_reweight.cu"]
+SOURCES = ["api.cu", "plan_kernels.cu", "attn_kernel.cu", "plan_static.cu", "spark_reweight.cu", "reblock.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [
     "-lineinfo",

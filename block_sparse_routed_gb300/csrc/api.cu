@@ -465,6 +465,53 @@ SA_API sa_status sparse_attn_spark_reweight(const sa_reweight_params* p, const v
   return SA_OK;
 }
 
+namespace {
+sa_status check_reblock(const sa_reblock_params* p) {
+  if (p == nullptr) return SA_EINVAL;
+  if (p->abi_version != SA_ABI_VERSION) return SA_EINVAL;
+  if (p->D != kHeadDim) return SA_EUNSUPPORTED;
+  if (p->T < 1 || p->H < 1) return SA_EINVAL;
+  if (p->fanout < 2 || p->fanout > kReblockMaxFanout || (p->fanout & (p->fanout - 1)) != 0) return SA_EINVAL;
+  if (p->landmarks < 2 || p->landmarks > kReblockMaxLandmarks) return SA_EINVAL;
+  if (p->token_stride < 0 || p->head_stride < 0 || p->token_stride % 8 != 0 || p->head_stride % 8 != 0)
+    return SA_EINVAL;
+  if (p->H > 65535 || int64_t(p->T) * p->H >= (int64_t(1) << 31)) return SA_EUNSUPPORTED;
+  return SA_OK;
+}
+}  // namespace
+
+SA_API sa_status sparse_attn_reblock_ws_bytes(const sa_reblock_params* p, uint64_t* out) {
+  if (out == nullptr) return SA_EINVAL;
+  const sa_status st = check_reblock(p);
+  if (st != SA_OK) return st;
+  *out = reblock_layout(p->T, p->H).total;
+  return SA_OK;
+}
+
+SA_API sa_status sparse_attn_spark_reblock(const sa_reblock_params* p, const void* x, int32_t* perm,
+                                           int32_t* inv, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  sa_status st = check_reblock(p);
+  if (st != SA_OK) return st;
+  if (!x || !perm || !inv || !ws) return SA_EINVAL;
+  if (!aligned(x, 16) || !aligned(perm, 4) || !aligned(inv, 4) || !aligned(ws, 256)) return SA_EINVAL;
+  if (ws_bytes < reblock_layout(p->T, p->H).total) return SA_EINVAL;
+  st = check_device();
+  if (st != SA_OK) return st;
+  ReblockArgs r;
+  r.x = static_cast<const uint16_t*>(x);
+  r.token_stride = p->token_stride;
+  r.head_stride = p->head_stride;
+  r.T = p->T;
+  r.H = p->H;
+  r.fanout = p->fanout;
+  r.landmarks = p->landmarks;
+  r.perm = perm;
+  r.inv = inv;
+  r.ws = ws;
+  if (cuda_failed(launch_reblock(r, stream))) return SA_ECUDA;
+  return SA_OK;
+}
+
 SA_API sa_status sparse_attn_last_device_status(const void* ws, cudaStream_t stream,
                                                 sa_status* out) {
   if (!ws || !out) return SA_EINVAL;

@@ -68,7 +68,8 @@ constexpr uint32_t kRegsSoftmax = 208;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "register split");
 constexpr int kTmemCols = 512;
 constexpr uint32_t kColO = 0;
-constexpr uint32_t kColS = 128;  // S buffer b at kColS + 128 b, b in {0, 1, 2}
+constexpr uint32_t kColS = 128;  // S buffer b at kColS + 128 b, b in {0, 1}
+constexpr uint32_t kColP = 384;  // P buffer b at kColP + 64 b (BF16 pairs), b in {0, 1}
 constexpr int kSlots = 4;        // K/V ring slots
 constexpr uint32_t kSlotBytes = 32768;  // K or V of 128 keys: 2 chunks x [128 rows x 128 B]
 constexpr uint32_t kQBytes = 32768;     // Q tile: 2 chunks x [128 rows x 128 B]
@@ -654,11 +655,10 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       auto vmaj_off = [](int kk) { return static_cast<uint64_t>((kk * 2048) >> 4); };
       auto slot_addr = [&](int q) { return sbase + kOffRing + (q % kSlots) * kSlotBytes; };
       auto wait_full = [&](int q) { return mbar_wait(bar(BAR_FULL + q % kSlots), (q / kSlots) & 1, kWaitLimitNs); };
-      auto s_col = [&](int gs) { return tmem + kColS + 128u * (gs % 3); };
-      // S_x reuses the buffer of P_{x-3}: PV_{x-3} must have completed.
-      auto wait_buffer_free = [&](int x) {
-        return x < 3 || mbar_wait(bar(BAR_PVDONE + (x - 3) % 3), ((x - 3) / 3) & 1, kWaitLimitNs);
-      };
+      // S_x reuses the buffer of S_{x-2}, which its softmax has read before
+      // releasing P_{x-2}: the PFULL wait of phase x-2 covers it.
+      auto s_col = [&](int gs) { return tmem + kColS + 128u * (gs & 1); };
+      auto p_col = [&](int gs) { return tmem + kColP + 64u * (gs & 1); };
       int seq = 0, G = 0;
       bool ok = true;
       for (int k = 0; ok; ++k) {
@@ -672,7 +672,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // prologue: S_G (and S_{G+1}), interleaved
         const int q0 = seq++;
         const int q1 = n > 1 ? seq++ : -1;
-        ok = wait_full(q0) && wait_buffer_free(G) && (q1 < 0 || (wait_full(q1) && wait_buffer_free(G + 1)));
+        ok = wait_full(q0) && (q1 < 0 || wait_full(q1));
         if (!ok) break;
         tc_fence_after();
         {
@@ -684,10 +684,10 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (q1 >= 0) umma_ss(s_col(G + 1), q_base + kmaj_off(kk), k1 + kmaj_off(kk), id_s, kk > 0 ? 1u : 0u);
           }
           umma_commit(bar(BAR_EMPTY + q0 % kSlots));
-          umma_commit(bar(BAR_SFULL + G % 3));
+          umma_commit(bar(BAR_SFULL + (G & 1)));
           if (q1 >= 0) {
             umma_commit(bar(BAR_EMPTY + q1 % kSlots));
-            umma_commit(bar(BAR_SFULL + (G + 1) % 3));
+            umma_commit(bar(BAR_SFULL + ((G + 1) & 1)));
           }
           if (n <= 2) umma_commit(bar(BAR_QEMPTY + slot));  // the unit's last S MMA
         }
@@ -697,35 +697,33 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           const bool has_k = j + 2 < n;
           const int qk = has_k ? seq++ : -1;
           if (!wait_full(qv)) { ok = false; break; }
-          if (!mbar_wait(bar(BAR_PFULL + gs % 3), (gs / 3) & 1, kWaitLimitNs)) { ok = false; break; }
+          if (!mbar_wait(bar(BAR_PFULL + (gs & 1)), (gs >> 1) & 1, kWaitLimitNs)) { ok = false; break; }
           // The unit's first PV overwrites O: the previous epilogue must be done.
           if (j == 0 && k >= 1 && !mbar_wait(bar(BAR_OEMPTY), (k - 1) & 1, kWaitLimitNs)) { ok = false; break; }
           tc_fence_after();
           const uint64_t vs = sdesc_sw128(slot_addr(qv), 16384, 1024);
-          const uint32_t pcol = s_col(gs);
-          // Two K-steps of PV first keep the pipe busy while PV_{g-1} drains.
-          umma_ts(tmem + kColO, pcol, vs + vmaj_off(0), id_o, j > 0 ? 1u : 0u);
-          umma_ts(tmem + kColO, pcol + 8, vs + vmaj_off(1), id_o, 1u);
+          const uint32_t pcol = p_col(gs);
           if (has_k) {
-            if (!wait_full(qk) || !wait_buffer_free(gs + 2)) { ok = false; break; }
+            if (!wait_full(qk)) { ok = false; break; }
             tc_fence_after();
             const uint64_t ks = sdesc_sw128(slot_addr(qk), 16, 1024);
             const uint32_t scol = s_col(gs + 2);
-            // S_{g+2} and the rest of PV_g alternate: two accumulators in flight.
+            // PV_g and S_{g+2} alternate K-steps: two accumulators in flight.
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
+              umma_ts(tmem + kColO, pcol + kk * 8, vs + vmaj_off(kk), id_o, (j > 0 || kk > 0) ? 1u : 0u);
               umma_ss(scol, q_base + kmaj_off(kk), ks + kmaj_off(kk), id_s, kk > 0 ? 1u : 0u);
-              if (kk < 6) umma_ts(tmem + kColO, pcol + (kk + 2) * 8, vs + vmaj_off(kk + 2), id_o, 1u);
             }
           } else {
 #pragma unroll
-            for (int kk = 2; kk < 8; ++kk) umma_ts(tmem + kColO, pcol + kk * 8, vs + vmaj_off(kk), id_o, 1u);
+            for (int kk = 0; kk < 8; ++kk)
+              umma_ts(tmem + kColO, pcol + kk * 8, vs + vmaj_off(kk), id_o, (j > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(bar(BAR_EMPTY + qv % kSlots));
-          umma_commit(bar(BAR_PVDONE + gs % 3));
+          umma_commit(bar(BAR_PVDONE + (gs & 1)));
           if (has_k) {
             umma_commit(bar(BAR_EMPTY + qk % kSlots));
-            umma_commit(bar(BAR_SFULL + (gs + 2) % 3));
+            umma_commit(bar(BAR_SFULL + (gs & 1)));
             if (j + 2 == n - 1) umma_commit(bar(BAR_QEMPTY + slot));  // the unit's last S MMA
           }
           if (*s_abort) { ok = false; break; }
@@ -770,11 +768,12 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       float l_run = 0.f;
       for (int j = ((G & 1) == grp) ? 0 : 1; j < n && ok; j += 2) {
         const int gs = G + j;
-        const int b = gs % 3;
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_SFULL + b), (gs / 3) & 1, kWaitLimitNs));
+        const int b = gs % 3;        // reference slot
+        const int sb = gs & 1;       // S and P buffers
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_SFULL + sb), (gs >> 1) & 1, kWaitLimitNs));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t scol = tmem + lane_addr + kColS + 128u * b;
+        const uint32_t scol = tmem + lane_addr + kColS + 128u * sb;
         // The two 64-key halves come from list entries 2j and 2j+1.  Pass 1
         // takes the row maximum over both halves, pass 2 reloads each half
         // from tensor memory and turns it into P (keeps 64 values live).
@@ -851,6 +850,11 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           my_ref = ref;
         }
         const float msub = (ref == -INFINITY) ? 0.f : ref;
+        // P_g goes where P_{g-2} was: PV_{g-2} must have completed.
+        if (gs >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_PVDONE + sb), ((gs - 2) >> 1) & 1, kWaitLimitNs))) {
+          ok = false;
+          break;
+        }
         uint64_t acc[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[q] = f2(0.f, 0.f);
@@ -900,8 +904,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
           }
           // P (BF16 pairs) of this half into columns [32 hh, 32 hh + 32) of
-          // S_g's buffer: columns already consumed by both passes of half 0.
-          tmem_st32(tmem + lane_addr + kColS + 128u * b + 32u * hh, p);
+          // P_g's buffer.
+          tmem_st32(tmem + lane_addr + kColP + 64u * sb + 32u * hh, p);
         }
         {
           float a0, a1, b0, b1, c0, c1, d0, d1;
@@ -916,7 +920,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // before P_g is released to the MMA thread.
         if (__any_sync(0xFFFFFFFFu, resc)) {
           // PV_{g-1} must have finished before O is rescaled (j >= 1 here).
-          if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_PVDONE + (gs - 1) % 3), ((gs - 1) / 3) & 1,
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_PVDONE + ((gs - 1) & 1)), ((gs - 1) >> 1) & 1,
                                                  kWaitLimitNs))) {
             ok = false;
             break;
@@ -936,7 +940,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(BAR_PFULL + b));
+        if (lane == 0) mbar_arrive(bar(BAR_PFULL + sb));
         if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) ok = false;
       }
       // ---- epilogue of the unit

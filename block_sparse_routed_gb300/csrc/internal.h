@@ -89,6 +89,29 @@ cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const
                              const CUtensorMap& tak, const CUtensorMap& tav, const AttnArgs& a,
                              cudaStream_t s);
 cudaError_t launch_spark_reweight(const ReweightArgs& r, cudaStream_t s);
+
+// Spark token reblocking (landmark tree).
+constexpr int kReblockMaxLandmarks = 64;
+constexpr int kReblockMaxFanout = 16;
+
+struct ReblockArgs {
+  const uint16_t* x;     // BF16 samples: row (t, h) at x + t * token_stride + h * head_stride
+  int64_t token_stride;  // elements
+  int64_t head_stride;   // elements
+  int T, H, fanout, landmarks;
+  int32_t* perm;         // [H, T]
+  int32_t* inv;          // [H, T]
+  void* ws;              // reblock_layout(T, H).total bytes, 256-byte aligned
+};
+
+struct ReblockLayout {
+  size_t xh, keys, ord0, ord1, total;  // byte offsets: FP16 unit rows [H, N, 128], keys [H, N], orders [H, N]
+};
+
+ReblockLayout reblock_layout(int T, int H);
+int reblock_depth(int m, int fanout);
+int reblock_launches(int T, int fanout);
+cudaError_t launch_reblock(const ReblockArgs& r, cudaStream_t s);
 int anchor_chunks(int Nv);
 cudaError_t launch_video_query_mean(const uint16_t* q, float* partial, uint16_t* anchor, int H, int Nv,
                                     cudaStream_t s);

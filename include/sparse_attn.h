@@ -255,6 +255,58 @@ sa_status sparse_attn_fused(const sa_params* p, const void* q, const void* k, co
                             size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * Spark token reblocking ("Sol-Attn and Spark for MiniMax-H3", section
+ * "Spark primitives", spark_reblock: a permutation of each head's tokens
+ * into 64-token blocks by a landmark tree, with its inverse; fanout with
+ * power-of-two scheduling and cosine scoring on normalized FP16 vectors from
+ * section "Spark inference integration").  The pages name the ingredients,
+ * not the steps; this call computes, per head h independently:
+ *   N = 64 floor(T / 64); tokens t >= N (the flat order's remainder) keep
+ *   their place at the end.  Each token is scored as its FP16 unit vector
+ *   (FP32 norm, zero rows stay zero).  The root node is [0, N) in flat
+ *   order; a node of m > 1 blocks splits into c children, c the largest
+ *   power of two <= min(fanout, m), child i taking floor(m / c) + [i < m % c]
+ *   blocks.  Its landmarks are the tokens at positions floor(j n / L),
+ *   j < L = min(landmarks, n), of its current order (n tokens); the pair
+ *   with the smallest cosine (ties to the lower (j, j')) gives a and b;
+ *   tokens ranked by (cos(t, a) - cos(t, b), position) fill child 0, 1, ...
+ *   in turn, and each child keeps the node's order.  Leaves are the blocks.
+ *   Cosines are FP32 sums of exact FP16 products in a fixed order (per
+ *   lane four consecutive terms left to right, then a butterfly over 32
+ *   lanes), so the integer result is reproducible bit for bit.
+ *   x      BF16 samples, row (t, h) at x + t * token_stride + h * head_stride
+ *          (elements; [1, T, H, 128] has token_stride = 128 H, head_stride =
+ *          128); 16-byte aligned, strides multiples of 8.  Read only.
+ *   perm   int32 [H, T]: perm[h, i] = original token at new position i;
+ *          the blocks are perm[h, 64 b : 64 b + 64], the excluded remainder
+ *          perm[h, N:].
+ *   inv    int32 [H, T]: inv[h, perm[h, i]] = i.
+ *   ws     workspace of sparse_attn_reblock_ws_bytes(p) bytes, 256-byte
+ *          aligned: FP16 unit rows [H, N, 128], keys uint64 [H, N], two
+ *          orders int32 [H, N] (each 256-byte aligned).  Owned by the caller.
+ * Errors before launch: SA_EINVAL (null params or pointer, abi_version
+ * mismatch, T < 1, H < 1, fanout not a power of two in [2, 16], landmarks
+ * outside [2, 64], a negative stride or one not a multiple of 8, x not
+ * 16-byte aligned, perm or inv not 4-byte aligned, ws not 256-byte aligned or
+ * short); SA_EUNSUPPORTED (D != 128, H > 65535, T * H >= 2^31, a device that
+ * is not sm_103).  SA_ECUDA if a launch fails.  Nothing is device-detected.
+ */
+typedef struct sa_reblock_params {
+  uint32_t abi_version; /* must be SA_ABI_VERSION                               */
+  int32_t T;            /* tokens, >= 1                                         */
+  int32_t H;            /* heads (independent sample matrices), >= 1            */
+  int32_t D;            /* feature dimension, must be 128                       */
+  int32_t fanout;       /* children per split at most: 2, 4, 8 or 16            */
+  int32_t landmarks;    /* landmarks per split, [2, 64] (32 by default)         */
+  int64_t token_stride; /* elements between tokens t and t + 1 of one head      */
+  int64_t head_stride;  /* elements between heads h and h + 1 of one token      */
+} sa_reblock_params;
+
+sa_status sparse_attn_reblock_ws_bytes(const sa_reblock_params* p, uint64_t* out);
+sa_status sparse_attn_spark_reblock(const sa_reblock_params* p, const void* x, int32_t* perm,
+                                    int32_t* inv, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * Reads the device status word of `ws` (written by the last plan or fwd
  * enqueued with it).  Synchronises `stream`.  SA_ECUDA if the copy fails.
  */

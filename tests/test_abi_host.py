@@ -199,3 +199,47 @@ def test_spark_reweight_rejects_bad_arguments_before_launch(native):
     assert call(params(), k=A + 8) == E
     assert call(params(), ak=A + 2) == E
     assert call(params(), lm=A + 2) == E
+
+
+def test_reblock_rejects_bad_arguments_before_launch(native):
+    """Argument errors of the reblocking entry point, all caught on the host."""
+    assert ctypes.sizeof(native.SaReblockParams) == 40
+    lib = native.load_library()
+    E, U = native.SA_EINVAL, native.SA_EUNSUPPORTED
+    A = 1 << 20
+
+    def params(T=1000, H=2, D=128, f=8, L=32, ts=256, hs=128, ver=None):
+        return native.SaReblockParams(native.SA_ABI_VERSION if ver is None else ver, T, H, D, f, L, ts, hs)
+
+    def call(p, x=A, perm=A, inv=A, ws=A, nbytes=1 << 40):
+        return lib.sparse_attn_spark_reblock(ctypes.byref(p), x, perm, inv, ws, nbytes, None)
+
+    def ws_bytes(p):
+        out = ctypes.c_uint64(0)
+        return lib.sparse_attn_reblock_ws_bytes(ctypes.byref(p), ctypes.byref(out)), out.value
+
+    assert lib.sparse_attn_spark_reblock(None, A, A, A, A, 1, None) == E
+    assert call(params(ver=2)) == E
+    assert call(params(D=64)) == U
+    assert call(params(T=0)) == E
+    assert call(params(H=0)) == E
+    for f in (0, 1, 3, 6, 32):
+        assert call(params(f=f)) == E
+    for L in (0, 1, 65):
+        assert call(params(L=L)) == E
+    assert call(params(ts=100)) == E
+    assert call(params(hs=-8)) == E
+    assert call(params(H=70000)) == U
+    assert call(params(T=1 << 26, H=64)) == U
+    assert call(params(), x=None) == E
+    assert call(params(), inv=None) == E
+    assert call(params(), x=A + 8) == E
+    assert call(params(), perm=A + 2) == E
+    assert call(params(), ws=A + 128) == E
+    st, need = ws_bytes(params())
+    assert st == native.SA_OK and need > 0
+    assert call(params(), nbytes=need - 1) == E
+    # N = 64 floor(T / 64) = 960: FP16 rows, keys, two orders, each 256-byte aligned
+    up = lambda b: (b + 255) // 256 * 256
+    assert need == up(960 * 2 * 256) + up(960 * 2 * 8) + 2 * up(960 * 2 * 4)
+    assert ws_bytes(params(T=40)) == (native.SA_OK, 0)
