@@ -93,6 +93,7 @@ cudaError_t launch_spark_reweight(const ReweightArgs& r, cudaStream_t s);
 // Spark token reblocking (landmark tree).
 constexpr int kReblockMaxLandmarks = 64;
 constexpr int kReblockMaxFanout = 16;
+constexpr int kReblockMaxLevelNodes = 2000;  // split nodes per launch (the list is a kernel parameter)
 
 struct ReblockArgs {
   const uint16_t* x;     // BF16 samples: row (t, h) at x + t * token_stride + h * head_stride
@@ -105,7 +106,8 @@ struct ReblockArgs {
 };
 
 struct ReblockLayout {
-  size_t xh, keys, ord0, ord1, total;  // byte offsets: FP16 unit rows [H, N, 128], keys [H, N], orders [H, N]
+  size_t xh, keys, ord0, ord1, pairs, total;  // byte offsets: FP16 unit rows [H, N, 128], keys [H, N],
+                                              // orders [H, N], landmark pairs int2 [H, N / 64]
 };
 
 ReblockLayout reblock_layout(int T, int H);

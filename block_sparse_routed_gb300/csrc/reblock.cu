@@ -12,15 +12,21 @@
 // tokens ranked by (kappa, position) are cut into the children, each of
 // which keeps the node's order.  The remainder tokens stay last.
 //
-// GPU shape: one launch normalises every token to an FP16 unit row; one
-// launch per tree level splits every node of that level for every head (a
-// CTA per node and head: landmark pair, keys, an 8-pass radix selection of
-// the child boundaries on unique 64-bit keys, then a stable scatter); a last
-// launch writes the permutation and its inverse.  All floating-point
-// decisions use explicit round-to-nearest FP32 operations in a fixed order,
-// so the integer result does not depend on the compiler's contractions.
+// GPU shape: one launch writes every token's FP16 unit row; three launches
+// per tree level follow: the farthest landmark pair of every split node (a
+// CTA per node and head; one Gram entry per thread), the keys of every token
+// of the level's split nodes (a warp per 64-token block, eight tokens in
+// flight, spread over the whole GPU), and per node an 8-bit radix selection
+// of the child boundaries on unique 64-bit keys followed by a stable scatter;
+// a last launch writes the permutation and its inverse.
+// All floating-point decisions use explicit round-to-nearest FP32 operations
+// in a fixed order, so the integer result does not depend on the compiler's
+// contractions.
 
 #include <cuda_fp16.h>
+
+#include <algorithm>
+#include <vector>
 
 #include "internal.h"
 
@@ -29,7 +35,8 @@ namespace {
 
 constexpr int kRbThreads = 512;
 constexpr int kRbWarps = kRbThreads / 32;
-constexpr int kUnitWarps = 8;
+constexpr int kPairThreads = 256;
+constexpr int kKeyTokens = 8;  // tokens in flight per warp in the keys kernel
 
 // Sum of a 128-term product held as four terms per lane: the lane's terms
 // left to right, then a butterfly over lane offsets 16, 8, 4, 2, 1 (every
@@ -43,16 +50,6 @@ __device__ __forceinline__ float fold128(float p0, float p1, float p2, float p3)
 
 __device__ __forceinline__ float dot128(const float a[4], const float b[4]) {
   return fold128(__fmul_rn(a[0], b[0]), __fmul_rn(a[1], b[1]), __fmul_rn(a[2], b[2]), __fmul_rn(a[3], b[3]));
-}
-
-__device__ __forceinline__ void load_half4(const __half* p, float v[4]) {
-  const uint2 raw = *reinterpret_cast<const uint2*>(p);
-  const __half2 lo = *reinterpret_cast<const __half2*>(&raw.x);
-  const __half2 hi = *reinterpret_cast<const __half2*>(&raw.y);
-  v[0] = __low2float(lo);
-  v[1] = __high2float(lo);
-  v[2] = __low2float(hi);
-  v[3] = __high2float(hi);
 }
 
 // Order-preserving 32-bit image of a finite float; -0 and +0 are one value.
@@ -92,206 +89,358 @@ __device__ __forceinline__ void find_node(int x, int m_root, int fanout, int lev
   leaf = m == 1;
 }
 
-// Warp per (token t < N, head h): the FP16 unit row of x[t, h] and the
-// identity order.  ss = sum of squares (exact squares of BF16 values), r =
-// sqrt(ss) and x / r rounded to nearest; a zero row stays zero.
-__global__ void __launch_bounds__(kUnitWarps * 32) reblock_unit_kernel(const uint16_t* __restrict__ x, int64_t ts,
-                                                                      int64_t hs, int N, int H,
-                                                                      __half* __restrict__ xh,
-                                                                      int32_t* __restrict__ ord) {
-  const int64_t w = static_cast<int64_t>(blockIdx.x) * kUnitWarps + threadIdx.x / 32;
-  const int lane = threadIdx.x % 32;
-  if (w >= static_cast<int64_t>(N) * H) return;
-  const int t = static_cast<int>(w / H), h = static_cast<int>(w % H);
-  const uint2 raw = *reinterpret_cast<const uint2*>(x + t * ts + h * hs + 4 * lane);
+// The same 128-term sum as fold128, by one thread over values in shared
+// memory: 32 partial sums of four products left to right, then the
+// butterfly's pairings (at offset o, partial l takes partial l + o), which
+// reproduce lane 0's operand order exactly.
+__device__ __forceinline__ float dot128_serial(const float* a, const float* b) {
+  float s[32];
+#pragma unroll
+  for (int l = 0; l < 32; ++l)
+    s[l] = __fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(a[4 * l], b[4 * l]), __fmul_rn(a[4 * l + 1], b[4 * l + 1])),
+                               __fmul_rn(a[4 * l + 2], b[4 * l + 2])),
+                     __fmul_rn(a[4 * l + 3], b[4 * l + 3]));
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+    for (int l = 0; l < o; ++l) s[l] = __fadd_rn(s[l], s[l + o]);
+  return s[0];
+}
+
+struct Samples {
+  const uint16_t* x;  // BF16
+  int64_t ts, hs;     // token and head strides (elements)
+  __device__ __forceinline__ uint2 raw(int t, int h, int lane) const {
+    return *reinterpret_cast<const uint2*>(x + t * ts + h * hs + 4 * lane);
+  }
+};
+
+// This lane's four values of the FP16 unit row of a BF16 row (held as four
+// per lane): ss = sum of squares (exact squares), r = sqrt(ss) and x / r
+// rounded to nearest FP32, then to FP16; a zero row stays zero.
+__device__ __forceinline__ void unit4(uint2 raw, float u[4]) {
   float v[4];
   v[0] = __uint_as_float(raw.x << 16);
   v[1] = __uint_as_float(raw.x & 0xFFFF0000u);
   v[2] = __uint_as_float(raw.y << 16);
   v[3] = __uint_as_float(raw.y & 0xFFFF0000u);
-  const float ss = dot128(v, v);
-  const float r = __fsqrt_rn(ss);
-  __half2 out[2];
-  float y[4];
+  const float r = __fsqrt_rn(dot128(v, v));
 #pragma unroll
-  for (int e = 0; e < 4; ++e) y[e] = r > 0.f ? __fdiv_rn(v[e], r) : 0.f;
-  out[0] = __halves2half2(__float2half_rn(y[0]), __float2half_rn(y[1]));
-  out[1] = __halves2half2(__float2half_rn(y[2]), __float2half_rn(y[3]));
-  const size_t row = static_cast<size_t>(h) * N + t;
-  *reinterpret_cast<uint2*>(xh + row * kHeadDim + 4 * lane) = *reinterpret_cast<const uint2*>(out);
-  if (lane == 0) ord[row] = t;
+  for (int e = 0; e < 4; ++e) u[e] = __half2float(__float2half_rn(r > 0.f ? __fdiv_rn(v[e], r) : 0.f));
 }
 
-// One tree level: CTA (x, h) splits the node of this depth whose first
-// block is x (or copies a finished leaf); other CTAs return at once.
-__global__ void __launch_bounds__(kRbThreads) reblock_level_kernel(const __half* __restrict__ xh,
-                                                                  const int32_t* __restrict__ ord_in,
-                                                                  int32_t* __restrict__ ord_out,
-                                                                  uint64_t* __restrict__ keys, int N, int fanout,
-                                                                  int L, int level) {
-  __shared__ __align__(16) __half land[kReblockMaxLandmarks][kHeadDim];
-  __shared__ float ua[kHeadDim], ub[kHeadDim];
-  __shared__ float wbest_c[kRbWarps];
-  __shared__ int wbest_p[kRbWarps];
-  __shared__ uint32_t hist[(kReblockMaxFanout - 1) * 256];
-  __shared__ uint64_t prefix[kReblockMaxFanout - 1];
-  __shared__ uint32_t rank[kReblockMaxFanout - 1];
-  __shared__ int wcnt[kRbWarps][kReblockMaxFanout];
-  __shared__ int running[kReblockMaxFanout], cstart[kReblockMaxFanout];
-  __shared__ int pair[2];
+__device__ __forceinline__ void load_half4(const __half* p, float v[4]) {
+  const uint2 raw = *reinterpret_cast<const uint2*>(p);
+  const __half2 lo = *reinterpret_cast<const __half2*>(&raw.x);
+  const __half2 hi = *reinterpret_cast<const __half2*>(&raw.y);
+  v[0] = __low2float(lo);
+  v[1] = __high2float(lo);
+  v[2] = __low2float(hi);
+  v[3] = __high2float(hi);
+}
 
-  const int x = blockIdx.x, h = blockIdx.y;
-  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+// FP16 unit rows of every token t < N of every head, [H, N, 128]: a warp per
+// eight tokens of one head, all eight rows in flight.
+__global__ void __launch_bounds__(256) reblock_unit_kernel(Samples xs, int N, int H, __half* __restrict__ xh) {
+  const int64_t w = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int groups = (N + kKeyTokens - 1) / kKeyTokens;
+  if (w >= static_cast<int64_t>(groups) * H) return;
+  const int h = static_cast<int>(w % H), t0 = static_cast<int>(w / H) * kKeyTokens;
+  uint2 raw[kKeyTokens];
+#pragma unroll
+  for (int u = 0; u < kKeyTokens; ++u) raw[u] = xs.raw(min(t0 + u, N - 1), h, lane);
+#pragma unroll
+  for (int u = 0; u < kKeyTokens; ++u) {
+    if (t0 + u >= N) break;
+    float v[4];
+    unit4(raw[u], v);
+    __half2 out[2];
+    out[0] = __floats2half2_rn(v[0], v[1]);  // exact: the values are FP16 already
+    out[1] = __floats2half2_rn(v[2], v[3]);
+    *reinterpret_cast<uint2*>(xh + (static_cast<size_t>(h) * N + t0 + u) * kHeadDim + 4 * lane) =
+        *reinterpret_cast<const uint2*>(out);
+  }
+}
+
+// Token at position i of the level's order (the root keeps the flat order).
+__device__ __forceinline__ int token_at(const int32_t* ord, size_t hb, int i, int level, int N) {
+  return level == 0 ? i : min(max(ord[hb + i], 0), N - 1);  // ids are < N; the clamp only bounds a bad order
+}
+
+// Split nodes of one tree level (their first blocks), passed by value.
+struct LevelNodes {
+  int count;
+  int start[kReblockMaxLevelNodes];
+};
+
+// The node of depth `level` that starts at block x (a split node).
+__device__ __forceinline__ int node_blocks(int x, int m_root, int fanout, int level) {
   int start, m;
   bool leaf;
-  find_node(x, N / kBlock, fanout, level, start, m, leaf);
-  if (start != x) return;
+  find_node(x, m_root, fanout, level, start, m, leaf);
+  return m;
+}
+
+// Farthest landmark pair of every split node of the level: CTA (k, h).  The
+// landmarks' unit rows go to shared memory (rows padded to 129 floats so a
+// warp reading different rows hits different banks); each thread takes Gram
+// entries in increasing pair number (pairs numbered in (j, j') order) and
+// keeps the smallest cosine with a strict <, so ties go to the lower pair.
+__global__ void __launch_bounds__(kPairThreads) reblock_pair_kernel(const __half* __restrict__ xh,
+                                                                   const int32_t* __restrict__ ord,
+                                                                   int2* __restrict__ pairs, int N, int fanout,
+                                                                   int L, int level,
+                                                                   const __grid_constant__ LevelNodes nodes) {
+  constexpr int kWarps = kPairThreads / 32;
+  extern __shared__ float land_raw[];  // [L][129]
+  auto land = [&](int j) { return land_raw + j * (kHeadDim + 1); };
+  __shared__ int ltok[kReblockMaxLandmarks];
+  __shared__ float bc_s[kPairThreads];
+  __shared__ int bp_s[kPairThreads];
+  const int x = nodes.start[blockIdx.x], h = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int m_root = N / kBlock;
+  const int n = kBlock * node_blocks(x, m_root, fanout, level);
   const size_t hb = static_cast<size_t>(h) * N;
-  const int n = kBlock * m;
-  const int32_t* src = ord_in + hb + static_cast<size_t>(kBlock) * start;
-  int32_t* dst = ord_out + hb + static_cast<size_t>(kBlock) * start;
-  uint64_t* key = keys + hb + static_cast<size_t>(kBlock) * start;
-  if (leaf) {
-    for (int i = tid; i < n; i += kRbThreads) dst[i] = src[i];
-    return;
+  const size_t nb0 = hb + static_cast<size_t>(kBlock) * x;  // the node's first position
+  const int nl = L < n ? L : n;
+  for (int j = warp; j < nl; j += kWarps) {
+    const int pos = static_cast<int>((static_cast<int64_t>(j) * n) / nl);
+    const int t = level == 0 ? kBlock * x + pos : token_at(ord, nb0, pos, 1, N);
+    float u[4];
+    load_half4(xh + (hb + t) * kHeadDim + 4 * lane, u);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) land(j)[4 * lane + e] = u[e];
+    if (lane == 0) ltok[j] = t;
   }
+  __syncthreads();
+  const int P = nl * (nl - 1) / 2;
+  float bc = 0.f;
+  int bp = -1;
+  for (int p = tid; p < P; p += kPairThreads) {
+    int j = 0, q = p;
+    while (q >= nl - 1 - j) {
+      q -= nl - 1 - j;
+      ++j;
+    }
+    const float cs = dot128_serial(land(j), land(j + 1 + q));
+    if (bp < 0 || cs < bc) {
+      bc = cs;
+      bp = p;
+    }
+  }
+  bc_s[tid] = bc;
+  bp_s[tid] = bp;
+  __syncthreads();
+  for (int w = kPairThreads / 2; w > 0; w >>= 1) {
+    if (tid < w) {
+      const int q = bp_s[tid + w];
+      if (q >= 0 && (bp_s[tid] < 0 || bc_s[tid + w] < bc_s[tid] || (bc_s[tid + w] == bc_s[tid] && q < bp_s[tid]))) {
+        bc_s[tid] = bc_s[tid + w];
+        bp_s[tid] = q;
+      }
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    int j = 0, q = bp_s[0];
+    while (q >= nl - 1 - j) {
+      q -= nl - 1 - j;
+      ++j;
+    }
+    pairs[static_cast<size_t>(h) * m_root + x] = make_int2(ltok[j], ltok[j + 1 + q]);
+  }
+}
+
+// Keys of every token in a split node of the level: warp per 64-token block
+// (16 blocks per CTA), eight tokens in flight per warp.  key = (order bits
+// of kappa) << 32 | position in the node, kappa = cos(t, a) - cos(t, b).
+__global__ void __launch_bounds__(kRbThreads) reblock_keys_kernel(const __half* __restrict__ xh,
+                                                                 const int32_t* __restrict__ ord,
+                                                                 const int2* __restrict__ pairs,
+                                                                 uint64_t* __restrict__ keys, int N, int fanout,
+                                                                 int level) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int x = blockIdx.x * kRbWarps + warp, h = blockIdx.y;
+  const int m_root = N / kBlock;
+  if (x >= m_root) return;
+  int start, m;
+  bool leaf;
+  find_node(x, m_root, fanout, level, start, m, leaf);
+  if (leaf) return;
+  const size_t hb = static_cast<size_t>(h) * N;
+  const int2 pr = pairs[static_cast<size_t>(h) * m_root + start];
+  float a[4], b[4];
+  load_half4(xh + (hb + min(max(pr.x, 0), N - 1)) * kHeadDim + 4 * lane, a);
+  load_half4(xh + (hb + min(max(pr.y, 0), N - 1)) * kHeadDim + 4 * lane, b);
+  const int p0 = kBlock * x;  // first position of the block in the head's order
+  const int t_lo = token_at(ord, hb, p0 + lane, level, N);
+  const int t_hi = token_at(ord, hb, p0 + 32 + lane, level, N);
+  const uint32_t pos0 = static_cast<uint32_t>(kBlock * (x - start));
+  for (int r0 = 0; r0 < kBlock; r0 += kKeyTokens) {
+    float v[kKeyTokens][4];
+#pragma unroll
+    for (int u = 0; u < kKeyTokens; ++u) {
+      const int r = r0 + u;
+      const int t = __shfl_sync(0xFFFFFFFFu, r < 32 ? t_lo : t_hi, r & 31);
+      load_half4(xh + (hb + t) * kHeadDim + 4 * lane, v[u]);
+    }
+    uint64_t mine = 0;
+#pragma unroll
+    for (int u = 0; u < kKeyTokens; ++u) {
+      const float kap = __fsub_rn(dot128(v[u], a), dot128(v[u], b));
+      if (lane == u) mine = (static_cast<uint64_t>(order_bits(kap)) << 32) | (pos0 + r0 + u);
+    }
+    if (lane < kKeyTokens) keys[hb + p0 + r0 + lane] = mine;
+  }
+}
+
+// Child boundaries and the stable scatter of every split node of the level:
+// CTA (k, h).  The keys of ranks cstart[1..c-1] are found by a radix
+// selection, 8 bits a pass from the top; boundaries whose prefixes agree
+// share a histogram (a key matches at most one prefix), increments are
+// aggregated per warp, and the passes stop once every boundary's bin holds
+// one key.
+template <int kT>
+__global__ void __launch_bounds__(kT) reblock_split_kernel(const int32_t* __restrict__ ord_in,
+                                                          int32_t* __restrict__ ord_out,
+                                                          const uint64_t* __restrict__ keys, int N, int fanout,
+                                                          int level, const __grid_constant__ LevelNodes nodes) {
+  constexpr int kNb = kReblockMaxFanout - 1;
+  constexpr int kW = kT / 32;
+  __shared__ uint32_t hist[kNb * 256];
+  __shared__ uint64_t prefix[kNb], gprefix[kNb], bound[kNb];
+  __shared__ uint32_t rank[kNb], bincnt[kNb];
+  __shared__ int bgroup[kNb];
+  __shared__ int ngroup, all_single;
+  __shared__ int wcnt[kW][kReblockMaxFanout];
+  __shared__ int running[kReblockMaxFanout], cstart[kReblockMaxFanout];
+
+  const int x = nodes.start[blockIdx.x], h = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int m = node_blocks(x, N / kBlock, fanout, level);
+  const int n = kBlock * m;
+  const size_t off = static_cast<size_t>(h) * N + static_cast<size_t>(kBlock) * x;
+  int32_t* dst = ord_out + off;
+  const uint64_t* key = keys + off;
   const int c = pow2_children(m, fanout);
   const int nb = c - 1;
-  const int nl = L < n ? L : n;
-
-  // Landmark rows.
-  for (int j = warp; j < nl; j += kRbWarps) {
-    const int pos = static_cast<int>((static_cast<int64_t>(j) * n) / nl);
-    const int t = min(max(src[pos], 0), N - 1);  // token ids are < N; the clamp only bounds a bad order
-    *reinterpret_cast<uint2*>(&land[j][4 * lane]) =
-        *reinterpret_cast<const uint2*>(xh + (hb + t) * kHeadDim + 4 * lane);
-  }
   if (tid < c) {
     const int base = m / c, extra = m % c;
     cstart[tid] = kBlock * (tid * base + (tid < extra ? tid : extra));
     running[tid] = 0;
   }
   __syncthreads();
-
-  // Farthest landmark pair: the smallest cosine, ties to the lower pair in
-  // (j, j') order (pairs are numbered in that order; each warp walks its
-  // share in increasing number, so a strict < keeps the lowest).
-  {
-    float bc = 0.f;
-    int bp = -1;
-    int p = 0;
-    for (int j = 0; j < nl; ++j) {
-      float a[4];
-      a[0] = __half2float(land[j][4 * lane]);
-      a[1] = __half2float(land[j][4 * lane + 1]);
-      a[2] = __half2float(land[j][4 * lane + 2]);
-      a[3] = __half2float(land[j][4 * lane + 3]);
-      for (int jj = j + 1; jj < nl; ++jj, ++p) {
-        if (p % kRbWarps != warp) continue;
-        float b[4];
-        b[0] = __half2float(land[jj][4 * lane]);
-        b[1] = __half2float(land[jj][4 * lane + 1]);
-        b[2] = __half2float(land[jj][4 * lane + 2]);
-        b[3] = __half2float(land[jj][4 * lane + 3]);
-        const float cs = dot128(a, b);
-        if (bp < 0 || cs < bc) {
-          bc = cs;
-          bp = p;
-        }
-      }
-    }
-    if (lane == 0) {
-      wbest_c[warp] = bc;
-      wbest_p[warp] = bp;
-    }
-  }
-  __syncthreads();
-  if (tid == 0) {
-    float bc = 0.f;
-    int bp = -1;
-    for (int w = 0; w < kRbWarps; ++w) {
-      const int p = wbest_p[w];
-      if (p < 0) continue;
-      if (bp < 0 || wbest_c[w] < bc || (wbest_c[w] == bc && p < bp)) {
-        bc = wbest_c[w];
-        bp = p;
-      }
-    }
-    int j = 0;
-    while (bp >= nl - 1 - j) {
-      bp -= nl - 1 - j;
-      ++j;
-    }
-    pair[0] = j;
-    pair[1] = j + 1 + bp;
-  }
-  __syncthreads();
-  if (tid < kHeadDim) {
-    ua[tid] = __half2float(land[pair[0]][tid]);
-    ub[tid] = __half2float(land[pair[1]][tid]);
-  }
-  __syncthreads();
-
-  // Keys: (order bits of kappa) << 32 | position, unique within the node.
-  {
-    float a[4], b[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      a[e] = ua[4 * lane + e];
-      b[e] = ub[4 * lane + e];
-    }
-    for (int i = warp; i < n; i += kRbWarps) {
-      const int t = min(max(src[i], 0), N - 1);
-      float v[4];
-      load_half4(xh + (hb + t) * kHeadDim + 4 * lane, v);
-      const float kap = __fsub_rn(dot128(v, a), dot128(v, b));
-      if (lane == 0) key[i] = (static_cast<uint64_t>(order_bits(kap)) << 32) | static_cast<uint32_t>(i);
-    }
-  }
   if (tid < nb) {
     prefix[tid] = 0;
     rank[tid] = static_cast<uint32_t>(cstart[tid + 1]);  // rank of child tid+1's first token
   }
-  __syncthreads();
-
-  // Radix selection of the keys of ranks cstart[1..c-1], 8 bits per pass.
-  for (int pass = 0; pass < 8; ++pass) {
+  int pass = 0;
+  for (;; ++pass) {
     const int shift = 56 - 8 * pass;
-    for (int e = tid; e < nb * 256; e += kRbThreads) hist[e] = 0u;
-    __syncthreads();
-    for (int i = tid; i < n; i += kRbThreads) {
-      const uint64_t k = key[i];
-      const uint32_t dig = static_cast<uint32_t>(k >> shift) & 255u;
-      for (int b = 0; b < nb; ++b)
-        if (pass == 0 || ((k ^ prefix[b]) >> (shift + 8)) == 0) atomicAdd(&hist[b * 256 + dig], 1u);
-    }
-    __syncthreads();
-    if (tid < nb) {
-      const uint32_t r = rank[tid];
-      uint32_t cum = 0;
-      int d = 0;
-      for (; d < 255; ++d) {
-        const uint32_t hc = hist[tid * 256 + d];
-        if (r < cum + hc) break;
-        cum += hc;
+    if (tid == 0) {
+      int ng = 0;
+      for (int b = 0; b < nb; ++b) {
+        int g = 0;
+        while (g < ng && gprefix[g] != prefix[b]) ++g;
+        if (g == ng) gprefix[ng++] = prefix[b];
+        bgroup[b] = g;
       }
-      prefix[tid] |= static_cast<uint64_t>(d) << shift;
-      rank[tid] = r - cum;
+      ngroup = ng;
     }
     __syncthreads();
+    const int ng = ngroup;
+    for (int e = tid; e < ng * 256; e += kT) hist[e] = 0u;
+    __syncthreads();
+    for (int i0 = 0; i0 < n; i0 += kT) {
+      const int i = i0 + tid;
+      int g = -1;
+      uint32_t dig = 0;
+      if (i < n) {
+        const uint64_t k = key[i];
+        dig = static_cast<uint32_t>(k >> shift) & 255u;
+        if (pass == 0) {
+          g = 0;
+        } else {
+          for (int q = 0; q < ng; ++q)
+            if (((k ^ gprefix[q]) >> (shift + 8)) == 0) {
+              g = q;
+              break;
+            }
+        }
+      }
+      const uint32_t tag = g >= 0 ? (static_cast<uint32_t>(g) << 8) | dig : 0x10000u | static_cast<uint32_t>(lane);
+      const unsigned peers = __match_any_sync(0xFFFFFFFFu, tag);
+      if (g >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[g * 256 + dig], static_cast<uint32_t>(__popc(peers)));
+    }
+    __syncthreads();
+    // boundary b's bin: a warp scans the 256 counts, eight per lane
+    for (int b = warp; b < nb; b += kW) {
+      const uint32_t* hg = hist + bgroup[b] * 256 + 8 * lane;
+      uint32_t c8[8], sum = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        c8[q] = hg[q];
+        sum += c8[q];
+      }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t excl = incl - sum, r = rank[b];
+      // the lane whose eight bins hold rank r (counts sum to more than r)
+      const unsigned hit = __ballot_sync(0xFFFFFFFFu, r >= excl && r < incl);
+      if (lane == __ffs(hit) - 1) {
+        uint32_t cum = excl, cnt = 0;
+        int sel = -1;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (sel < 0 && (q == 7 || r < cum + c8[q])) {
+            sel = q;
+            cnt = c8[q];
+          } else if (sel < 0) {
+            cum += c8[q];
+          }
+        }
+        prefix[b] |= static_cast<uint64_t>(8 * lane + sel) << shift;
+        rank[b] = r - cum;
+        bincnt[b] = cnt;
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int one = 1;
+      for (int b = 0; b < nb; ++b) one &= bincnt[b] == 1u ? 1 : 0;
+      all_single = one;
+    }
+    __syncthreads();
+    if (all_single || pass == 7) break;
   }
+  // The single key of each boundary's bin is the boundary key.
+  {
+    const int shift = 56 - 8 * pass;
+    for (int i = tid; i < n; i += kT) {
+      const uint64_t k = key[i];
+      for (int b = 0; b < nb; ++b)
+        if ((k >> shift) == (prefix[b] >> shift)) bound[b] = k;
+    }
+  }
+  __syncthreads();
 
   // Stable scatter: child = number of boundary keys <= the token's key;
   // inside a child, tokens keep the node's order.
   const unsigned lt = (1u << lane) - 1u;
-  for (int c0 = 0; c0 < n; c0 += kRbThreads) {
+  for (int c0 = 0; c0 < n; c0 += kT) {
     const int i = c0 + tid;
     const bool in = i < n;
     int ch = 0, t = 0;
     if (in) {
       const uint64_t k = key[i];
-      for (int b = 0; b < nb; ++b) ch += k >= prefix[b] ? 1 : 0;
-      t = src[i];
+      for (int b = 0; b < nb; ++b) ch += k >= bound[b] ? 1 : 0;
+      t = level == 0 ? kBlock * x + i : ord_in[off + i];
     }
     int my = 0;
     for (int b = 0; b < c; ++b) {
@@ -302,7 +451,7 @@ __global__ void __launch_bounds__(kRbThreads) reblock_level_kernel(const __half*
     __syncthreads();
     if (tid < c) {
       int run = running[tid];
-      for (int w = 0; w < kRbWarps; ++w) {
+      for (int w = 0; w < kW; ++w) {
         const int v = wcnt[w][tid];
         wcnt[w][tid] = run;
         run += v;
@@ -317,13 +466,30 @@ __global__ void __launch_bounds__(kRbThreads) reblock_level_kernel(const __half*
 }
 
 // perm[h, i] = token at new position i (the remainder keeps its place at the
-// end); inv[h, perm[h, i]] = i.
-__global__ void reblock_finish_kernel(const int32_t* __restrict__ ord, int N, int T, int H,
-                                      int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+// end); inv[h, perm[h, i]] = i.  A block's final order sits in the buffer its
+// leaf was written to: the one of the parity of the leaf's depth (depth 0,
+// a root of one block, is the flat order).
+__global__ void reblock_finish_kernel(const int32_t* __restrict__ ord0, const int32_t* __restrict__ ord1, int N,
+                                      int T, int H, int fanout, int32_t* __restrict__ perm,
+                                      int32_t* __restrict__ inv) {
   const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (e >= static_cast<int64_t>(T) * H) return;
   const int h = static_cast<int>(e / T), i = static_cast<int>(e % T);
-  const int t = i < N ? ord[static_cast<size_t>(h) * N + i] : i;
+  int t = i;
+  if (i < N) {
+    const int x = i / kBlock, m_root = N / kBlock;
+    int start = 0, m = m_root, d = 0;
+    while (m > 1) {
+      const int c = pow2_children(m, fanout);
+      const int base = m / c, extra = m % c;
+      const int o = x - start;
+      const int j = o < extra * (base + 1) ? o / (base + 1) : extra + (o - extra * (base + 1)) / base;
+      start += j * base + (j < extra ? j : extra);
+      m = base + (j < extra ? 1 : 0);
+      ++d;
+    }
+    if (d > 0) t = ((d & 1) ? ord1 : ord0)[static_cast<size_t>(h) * N + i];  // a root leaf keeps the flat order
+  }
   perm[e] = t;
   if (t >= 0 && t < T) inv[static_cast<size_t>(h) * T + t] = i;
 }
@@ -353,41 +519,103 @@ ReblockLayout reblock_layout(int T, int H) {
   off += up(N * H * 4);
   l.ord1 = off;
   off += up(N * H * 4);
+  l.pairs = off;
+  off += up((N / kBlock) * H * 8);
   l.total = off;
   return l;
 }
 
+namespace {
+// First blocks of the split nodes of depth `level` (host copy of the walk).
+std::vector<int> level_nodes(int m_root, int fanout, int level, int* max_m = nullptr) {
+  std::vector<int> out;
+  if (max_m) *max_m = 0;
+  for (int x = 0; x < m_root; ++x) {
+    int start = 0, m = m_root;
+    bool leaf = false;
+    for (int d = 0; d < level && !leaf; ++d) {
+      if (m == 1) {
+        leaf = true;
+        break;
+      }
+      const int c = pow2_children(m, fanout);
+      const int base = m / c, extra = m % c;
+      const int o = x - start;
+      const int i = o < extra * (base + 1) ? o / (base + 1) : extra + (o - extra * (base + 1)) / base;
+      start += i * base + (i < extra ? i : extra);
+      m = base + (i < extra ? 1 : 0);
+    }
+    if (!leaf && m > 1 && start == x) {
+      out.push_back(x);
+      if (max_m && m > *max_m) *max_m = m;
+    }
+  }
+  return out;
+}
+}  // namespace
+
 cudaError_t launch_reblock(const ReblockArgs& r, cudaStream_t stream) {
   const int N = kBlock * (r.T / kBlock);
+  const int m_root = N / kBlock;
   const ReblockLayout l = reblock_layout(r.T, r.H);
   char* ws = static_cast<char*>(r.ws);
-  __half* xh = reinterpret_cast<__half*>(ws + l.xh);
   uint64_t* keys = reinterpret_cast<uint64_t*>(ws + l.keys);
   int32_t* ord[2] = {reinterpret_cast<int32_t*>(ws + l.ord0), reinterpret_cast<int32_t*>(ws + l.ord1)};
-  int depth = 0;
-  if (N > 0) {
-    const int64_t warps = static_cast<int64_t>(N) * r.H;
-    reblock_unit_kernel<<<static_cast<unsigned>((warps + kUnitWarps - 1) / kUnitWarps), kUnitWarps * 32, 0, stream>>>(
-        r.x, r.token_stride, r.head_stride, N, r.H, xh, ord[0]);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    depth = reblock_depth(N / kBlock, r.fanout);
-    for (int lv = 0; lv < depth; ++lv) {
-      reblock_level_kernel<<<dim3(N / kBlock, r.H), kRbThreads, 0, stream>>>(xh, ord[lv & 1], ord[(lv + 1) & 1], keys,
-                                                                             N, r.fanout, r.landmarks, lv);
-      e = cudaGetLastError();
-      if (e != cudaSuccess) return e;
+  int2* pairs = reinterpret_cast<int2*>(ws + l.pairs);
+  __half* xh = reinterpret_cast<__half*>(ws + l.xh);
+  const Samples xs{r.x, r.token_stride, r.head_stride};
+  cudaError_t e;
+  const int depth = N > 0 ? reblock_depth(m_root, r.fanout) : 0;
+  if (depth > 0) {
+    const int64_t warps = static_cast<int64_t>((N + kKeyTokens - 1) / kKeyTokens) * r.H;
+    reblock_unit_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(xs, N, r.H, xh);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  for (int lv = 0; lv < depth; ++lv) {
+    int max_m = 0;
+    const std::vector<int> all = level_nodes(m_root, r.fanout, lv, &max_m);
+    const bool small = kBlock * max_m <= 1024;  // levels of small nodes get small CTAs
+    for (int pass = 0; pass < 3; ++pass) {
+      if (pass == 1) {
+        reblock_keys_kernel<<<dim3((m_root + kRbWarps - 1) / kRbWarps, r.H), kRbThreads, 0, stream>>>(
+            xh, ord[lv & 1], pairs, keys, N, r.fanout, lv);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        continue;
+      }
+      for (size_t k0 = 0; k0 < all.size(); k0 += kReblockMaxLevelNodes) {
+        LevelNodes nodes;
+        nodes.count = static_cast<int>(std::min<size_t>(kReblockMaxLevelNodes, all.size() - k0));
+        for (int k = 0; k < nodes.count; ++k) nodes.start[k] = all[k0 + k];
+        const dim3 grid(nodes.count, r.H);
+        if (pass == 0)
+          reblock_pair_kernel<<<grid, kPairThreads, r.landmarks * (kHeadDim + 1) * sizeof(float), stream>>>(
+              xh, ord[lv & 1], pairs, N, r.fanout, r.landmarks, lv, nodes);
+        else if (small)
+          reblock_split_kernel<128><<<grid, 128, 0, stream>>>(ord[lv & 1], ord[(lv + 1) & 1], keys, N, r.fanout,
+                                                             lv, nodes);
+        else
+          reblock_split_kernel<512><<<grid, 512, 0, stream>>>(ord[lv & 1], ord[(lv + 1) & 1], keys, N, r.fanout,
+                                                             lv, nodes);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      }
     }
   }
   const int64_t total = static_cast<int64_t>(r.T) * r.H;
-  reblock_finish_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(ord[depth & 1], N, r.T, r.H,
-                                                                                       r.perm, r.inv);
+  reblock_finish_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(ord[0], ord[1], N, r.T, r.H,
+                                                                                       r.fanout, r.perm, r.inv);
   return cudaGetLastError();
 }
 
 int reblock_launches(int T, int fanout) {
-  const int N = kBlock * (T / kBlock);
-  return N > 0 ? 2 + reblock_depth(N / kBlock, fanout) : 1;
+  const int m_root = T / kBlock;
+  if (m_root == 0) return 1;
+  const int depth = reblock_depth(m_root, fanout);
+  int n = 2 + depth;  // unit rows, finish, keys per level
+  for (int lv = 0; lv < depth; ++lv) {
+    const int k = static_cast<int>(level_nodes(m_root, fanout, lv).size());
+    n += 2 * ((k + kReblockMaxLevelNodes - 1) / kReblockMaxLevelNodes);
+  }
+  return n;
 }
 
 }  // namespace sa

@@ -283,7 +283,8 @@ sa_status sparse_attn_fused(const sa_params* p, const void* q, const void* k, co
  *   inv    int32 [H, T]: inv[h, perm[h, i]] = i.
  *   ws     workspace of sparse_attn_reblock_ws_bytes(p) bytes, 256-byte
  *          aligned: FP16 unit rows [H, N, 128], keys uint64 [H, N], two
- *          orders int32 [H, N] (each 256-byte aligned).  Owned by the caller.
+ *          orders int32 [H, N], landmark pairs int32 [H, N / 64, 2] (each
+ *          256-byte aligned).  Owned by the caller.
  * Errors before launch: SA_EINVAL (null params or pointer, abi_version
  * mismatch, T < 1, H < 1, fanout not a power of two in [2, 16], landmarks
  * outside [2, 64], a negative stride or one not a multiple of 8, x not

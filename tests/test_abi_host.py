@@ -239,7 +239,8 @@ def test_reblock_rejects_bad_arguments_before_launch(native):
     st, need = ws_bytes(params())
     assert st == native.SA_OK and need > 0
     assert call(params(), nbytes=need - 1) == E
-    # N = 64 floor(T / 64) = 960: FP16 rows, keys, two orders, each 256-byte aligned
+    # N = 64 floor(T / 64) = 960: FP16 rows, keys, two orders, landmark
+    # pairs of the 15 blocks, each 256-byte aligned
     up = lambda b: (b + 255) // 256 * 256
-    assert need == up(960 * 2 * 256) + up(960 * 2 * 8) + 2 * up(960 * 2 * 4)
+    assert need == up(960 * 2 * 256) + up(960 * 2 * 8) + 2 * up(960 * 2 * 4) + up(15 * 2 * 8)
     assert ws_bytes(params(T=40)) == (native.SA_OK, 0)
