@@ -100,7 +100,7 @@ enum {
   BAR_EMPTY = 8,     // +ring slot
   BAR_SFULL = 12,    // +buffer (3)
   BAR_PFULL = 15,    // +buffer
-  BAR_PVDONE = 18,   // +buffer
+  BAR_PVDONE = 18,   // PV of a unit's step n-2 completed (once per unit of n >= 2 steps)
   BAR_MREADY = 21,   // +buffer: reference of that step published
   BAR_OFULL = 24,    // the unit's last PV completed
   BAR_OEMPTY = 25,   // the epilogue has read O
@@ -720,7 +720,9 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
               umma_ts(tmem + kColO, pcol + kk * 8, vs + vmaj_off(kk), id_o, (j > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(bar(BAR_EMPTY + qv % kSlots));
-          umma_commit(bar(BAR_PVDONE + (gs & 1)));
+          // The softmax of step g waits for PV_{g-1} only to rescale O; for
+          // g < n-1 the commit of S_{g+1} (after PV_{g-1}) already says so.
+          if (j == n - 2) umma_commit(bar(BAR_PVDONE));
           if (has_k) {
             umma_commit(bar(BAR_EMPTY + qk % kSlots));
             umma_commit(bar(BAR_SFULL + (gs & 1)));
@@ -752,6 +754,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     float* rref = xchg;                    // [3][128]: reference after step g at g % 3
     float* xl = xchg + 3 * 128;            // [2][128]: partial row sums
     int G = 0;
+    int pv_units = 0;  // units of n >= 2 steps before this one (PV-done commits)
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int slot = k & 1;
@@ -850,11 +853,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           my_ref = ref;
         }
         const float msub = (ref == -INFINITY) ? 0.f : ref;
-        // P_g goes where P_{g-2} was: PV_{g-2} must have completed.
-        if (gs >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_PVDONE + sb), ((gs - 2) >> 1) & 1, kWaitLimitNs))) {
-          ok = false;
-          break;
-        }
+        // P_g goes where P_{g-2} was: PV_{g-2} has completed, since S_g was
+        // committed after it.
         uint64_t acc[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[q] = f2(0.f, 0.f);
@@ -919,9 +919,13 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // O holds sum_{i<g} P_i V_i relative to `prev`; move it to `ref`
         // before P_g is released to the MMA thread.
         if (__any_sync(0xFFFFFFFFu, resc)) {
-          // PV_{g-1} must have finished before O is rescaled (j >= 1 here).
-          if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_PVDONE + ((gs - 1) & 1)), ((gs - 1) >> 1) & 1,
-                                                 kWaitLimitNs))) {
+          // PV_{g-1} must have finished before O is rescaled (j >= 1 here):
+          // S_{g+1} was committed after it, or, for the unit's last step, the
+          // unit's PV-done commit (step n-2) says so.
+          const bool via_s = j + 1 < n;
+          const uint32_t wb = via_s ? bar(BAR_SFULL + ((gs + 1) & 1)) : bar(BAR_PVDONE);
+          const uint32_t wp = via_s ? (((gs + 1) >> 1) & 1) : static_cast<uint32_t>(pv_units & 1);
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(wb, wp, kWaitLimitNs))) {
             ok = false;
             break;
           }
@@ -1001,6 +1005,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       }
       ok = !named_bar_or(2, kSoftmaxThreads, *s_abort != 0);
       G += n;
+      if (n >= 2) ++pv_units;
     }
     if (!ok) {
       *s_abort = 1;
