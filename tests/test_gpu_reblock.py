@@ -79,6 +79,14 @@ def test_h3_queries_sampled_heads_fanout16(bsr):
     _check(bsr, arrays["q"], 16, heads=[0, 17, 38, 55])
 
 
+@pytest.mark.parametrize("name,heads", [("32k", [0, 39]), ("64k", [0, 23])])
+def test_largest_configs_sampled_heads(bsr, name, heads):
+    # the largest sizes (64k: a root of 1056 blocks, one CTA per head selects
+    # its boundaries among 67584 keys), every head computed, two compared
+    arrays, _ = make_workload(name)
+    _check(bsr, arrays["k"], 8, heads=heads)
+
+
 def test_8k_keys(bsr):
     arrays, _ = make_workload("8k")
     _check(bsr, arrays["k"], 8, heads=[0, 5, 11, 23])

@@ -59,6 +59,11 @@ def _rank_main(rank, world, port, q):
         parts = [None] * world
         dist.all_gather_object(parts, (mine, ref["idx"], ref["cnt"], o))
         out["parts"] = parts
+        # reblocking of this rank's heads (independent per head as well)
+        rb = O.spark_reblock(kh, 4)
+        rparts = [None] * world
+        dist.all_gather_object(rparts, (mine, rb["perm"], rb["inv"]))
+        out["rparts"] = rparts
         out["H"] = prm["H"]
         q.put((rank, out))
     finally:
@@ -118,6 +123,21 @@ def test_heads_split_across_ranks_give_the_single_process_result(two_ranks):
                 assert np.array_equal(cnt[j], ref["cnt"][h])
                 assert np.array_equal(oh[:, j], o[:, h])
         assert sorted(seen) == list(range(two_ranks[r]["H"]))
+
+
+def test_reblocking_heads_split_across_ranks(two_ranks):
+    import oracle as O
+    from workloads import make_workload
+
+    arrays, prm = make_workload("tiny")
+    rb = O.spark_reblock(arrays["k"], 4)
+    for r in (0, 1):
+        seen = []
+        for heads, perm, inv in two_ranks[r]["rparts"]:
+            for j, h in enumerate(heads):
+                seen.append(h)
+                assert np.array_equal(perm[j], rb["perm"][h]) and np.array_equal(inv[j], rb["inv"][h])
+        assert sorted(seen) == list(range(prm["H"]))
 
 
 def test_reference_arm_runs_on_rank_zero_only(capsys):
