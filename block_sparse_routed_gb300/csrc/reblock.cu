@@ -36,6 +36,7 @@ namespace {
 constexpr int kRbThreads = 512;
 constexpr int kRbWarps = kRbThreads / 32;
 constexpr int kPairThreads = 256;
+constexpr int kLandStride = kHeadDim + 4;  // floats per landmark row in shared memory
 constexpr int kKeyTokens = 8;  // tokens in flight per warp in the keys kernel
 
 // Sum of a 128-term product held as four terms per lane: the lane's terms
@@ -96,10 +97,12 @@ __device__ __forceinline__ void find_node(int x, int m_root, int fanout, int lev
 __device__ __forceinline__ float dot128_serial(const float* a, const float* b) {
   float s[32];
 #pragma unroll
-  for (int l = 0; l < 32; ++l)
-    s[l] = __fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(a[4 * l], b[4 * l]), __fmul_rn(a[4 * l + 1], b[4 * l + 1])),
-                               __fmul_rn(a[4 * l + 2], b[4 * l + 2])),
-                     __fmul_rn(a[4 * l + 3], b[4 * l + 3]));
+  for (int l = 0; l < 32; ++l) {
+    const float4 x = *reinterpret_cast<const float4*>(a + 4 * l);
+    const float4 y = *reinterpret_cast<const float4*>(b + 4 * l);
+    s[l] = __fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(x.x, y.x), __fmul_rn(x.y, y.y)), __fmul_rn(x.z, y.z)),
+                     __fmul_rn(x.w, y.w));
+  }
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1)
 #pragma unroll
@@ -193,8 +196,10 @@ __global__ void __launch_bounds__(kPairThreads) reblock_pair_kernel(const __half
                                                                    int L, int level,
                                                                    const __grid_constant__ LevelNodes nodes) {
   constexpr int kWarps = kPairThreads / 32;
-  extern __shared__ float land_raw[];  // [L][129]
-  auto land = [&](int j) { return land_raw + j * (kHeadDim + 1); };
+  // [L][132]: 16-byte rows for vector loads; 132 = 4 mod 32 words keeps the
+  // eight rows a quarter-warp reads in distinct banks
+  extern __shared__ __align__(16) float land_raw[];
+  auto land = [&](int j) { return land_raw + j * kLandStride; };
   __shared__ int ltok[kReblockMaxLandmarks];
   __shared__ float bc_s[kPairThreads];
   __shared__ int bp_s[kPairThreads];
@@ -574,7 +579,7 @@ cudaError_t launch_reblock(const ReblockArgs& r, cudaStream_t stream) {
   for (int lv = 0; lv < depth; ++lv) {
     int max_m = 0;
     const std::vector<int> all = level_nodes(m_root, r.fanout, lv, &max_m);
-    const bool small = kBlock * max_m <= 1024;  // levels of small nodes get small CTAs
+    const int threads = kBlock * max_m <= 1024 ? 128 : (kBlock * max_m <= 4096 ? 512 : 1024);
     for (int pass = 0; pass < 3; ++pass) {
       if (pass == 1) {
         reblock_keys_kernel<<<dim3((m_root + kRbWarps - 1) / kRbWarps, r.H), kRbThreads, 0, stream>>>(
@@ -588,14 +593,17 @@ cudaError_t launch_reblock(const ReblockArgs& r, cudaStream_t stream) {
         for (int k = 0; k < nodes.count; ++k) nodes.start[k] = all[k0 + k];
         const dim3 grid(nodes.count, r.H);
         if (pass == 0)
-          reblock_pair_kernel<<<grid, kPairThreads, r.landmarks * (kHeadDim + 1) * sizeof(float), stream>>>(
+          reblock_pair_kernel<<<grid, kPairThreads, r.landmarks * kLandStride * sizeof(float), stream>>>(
               xh, ord[lv & 1], pairs, N, r.fanout, r.landmarks, lv, nodes);
-        else if (small)
+        else if (threads == 128)  // CTA size follows the level's node size
           reblock_split_kernel<128><<<grid, 128, 0, stream>>>(ord[lv & 1], ord[(lv + 1) & 1], keys, N, r.fanout,
                                                              lv, nodes);
-        else
+        else if (threads == 512)
           reblock_split_kernel<512><<<grid, 512, 0, stream>>>(ord[lv & 1], ord[(lv + 1) & 1], keys, N, r.fanout,
                                                              lv, nodes);
+        else
+          reblock_split_kernel<1024><<<grid, 1024, 0, stream>>>(ord[lv & 1], ord[(lv + 1) & 1], keys, N, r.fanout,
+                                                               lv, nodes);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
       }
     }
