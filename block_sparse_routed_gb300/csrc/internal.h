@@ -112,7 +112,6 @@ struct ReblockLayout {
 
 ReblockLayout reblock_layout(int T, int H);
 int reblock_depth(int m, int fanout);
-int reblock_launches(int T, int fanout);
 cudaError_t launch_reblock(const ReblockArgs& r, cudaStream_t s);
 int anchor_chunks(int Nv);
 cudaError_t launch_video_query_mean(const uint16_t* q, float* partial, uint16_t* anchor, int H, int Nv,

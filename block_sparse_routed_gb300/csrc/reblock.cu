@@ -614,16 +614,4 @@ cudaError_t launch_reblock(const ReblockArgs& r, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-int reblock_launches(int T, int fanout) {
-  const int m_root = T / kBlock;
-  if (m_root == 0) return 1;
-  const int depth = reblock_depth(m_root, fanout);
-  int n = 2 + depth;  // unit rows, finish, keys per level
-  for (int lv = 0; lv < depth; ++lv) {
-    const int k = static_cast<int>(level_nodes(m_root, fanout, lv).size());
-    n += 2 * ((k + kReblockMaxLevelNodes - 1) / kReblockMaxLevelNodes);
-  }
-  return n;
-}
-
 }  // namespace sa
