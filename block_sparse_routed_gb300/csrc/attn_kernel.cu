@@ -27,20 +27,20 @@
 // ring, the S buffers and every barrier phase continue across units, so the
 // next unit's loads and first MMAs overlap the current unit's tail.
 //
-// Schedule.  A tcgen05.mma that accumulates into the same tensor-memory tile
-// as the instruction issued just before it stalls the issuing thread, while
-// alternating two independent accumulators keeps the tensor pipe full.  So in
-// phase g (a global step index) the MMA thread interleaves the K-steps of
-// PV_g (O += P_g V_g) and of S_{g+2} = Q K_{g+2}^T.  Three S buffers make that
-// possible; P_g is written as packed BF16 over the first 64 columns of S_g's
-// buffer.  S_{g+2} reuses the buffer of P_{g-1}, so it waits for PV_{g-1} to
-// complete; two K-steps of PV_g are issued before that wait to keep the pipe
-// busy.
+// Schedule.  One thread issues tcgen05.mma at about one instruction per 105
+// cycles at this shape (M = N = 128, K = 16), slower than the tensor pipe
+// executes them (64), so two threads issue: warp 1 the S MMAs
+// (S_x = Q K_x^T) and warp 3 the PV MMAs (O += P_x V_x), each a chain on its
+// own accumulator.  Three S buffers (step x in buffer x mod 3) give the
+// softmax two steps of lead: S_{x+3} is issued as soon as PV_x has completed,
+// since P_x is written as packed BF16 over the first 64 columns of S_x's
+// buffer.
 //
 // Warp roles (12 warps, three warpgroups): warpgroup 0 holds the
 // single-thread roles: warp 0 issues TMA loads (Q per unit; K and V per step
-// through a 4-slot ring), warp 1 owns tensor memory and issues the MMAs (one
-// thread), warp 2 schedules units and merges their block lists, warp 3 idles.
+// through a 4-slot ring), warp 1 owns tensor memory and issues the S MMAs,
+// warp 2 schedules units and merges their block lists, warp 3 issues the PV
+// MMAs.
 // Warpgroups 1 (warps 4-7, softmax group 0) and 2 (warps 8-11, group 1) each
 // own one query row per thread (= tensor-memory lane); group 0 takes even
 // global steps and group 1 odd ones, all 128 columns each, so two steps'
@@ -68,8 +68,7 @@ constexpr uint32_t kRegsSoftmax = 208;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "register split");
 constexpr int kTmemCols = 512;
 constexpr uint32_t kColO = 0;
-constexpr uint32_t kColS = 128;  // S buffer b at kColS + 128 b, b in {0, 1}
-constexpr uint32_t kColP = 384;  // P buffer b at kColP + 64 b (BF16 pairs), b in {0, 1}
+constexpr uint32_t kColS = 128;  // S buffer b at kColS + 128 b, b in {0, 1, 2}; P_x over S_x's first 64
 constexpr int kSlots = 4;        // K/V ring slots
 constexpr uint32_t kSlotBytes = 32768;  // K or V of 128 keys: 2 chunks x [128 rows x 128 B]
 constexpr uint32_t kQBytes = 32768;     // Q tile: 2 chunks x [128 rows x 128 B]
@@ -100,14 +99,15 @@ enum {
   BAR_EMPTY = 8,     // +ring slot
   BAR_SFULL = 12,    // +buffer (3)
   BAR_PFULL = 15,    // +buffer
-  BAR_PVDONE = 18,   // PV of a unit's step n-2 completed (once per unit of n >= 2 steps)
+  BAR_PVDONE = 18,   // +buffer: PV of that step completed
   BAR_MREADY = 21,   // +buffer: reference of that step published
   BAR_OFULL = 24,    // the unit's last PV completed
   BAR_OEMPTY = 25,   // the epilogue has read O
   BAR_UFULL = 26,    // +slot (2): unit descriptor ready
   BAR_UEMPTY = 28,   // +slot: every role is done with the descriptor
-  BAR_DRAIN = 30,
-  NUM_BARS = 31
+  BAR_DRAIN = 30,    // the S issuer's MMAs drained (abort)
+  BAR_DRAIN2 = 31,   // the PV issuer's MMAs drained (abort)
+  NUM_BARS = 32
 };
 static_assert(NUM_BARS * 8 <= 512, "barrier area");
 
@@ -275,7 +275,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     for (int b = 0; b < 3; ++b) mbar_init(bar(BAR_PFULL + b), 4);   // the owning group's 4 warps
     for (int b = 0; b < 3; ++b) mbar_init(bar(BAR_MREADY + b), 4);
     mbar_init(bar(BAR_OEMPTY), 8);                                   // all softmax warps
-    for (int s = 0; s < 2; ++s) mbar_init(bar(BAR_UEMPTY + s), 10);  // producer + MMA + 8 softmax
+    for (int s = 0; s < 2; ++s) mbar_init(bar(BAR_UEMPTY + s), 11);  // producer + 2 MMA issuers + 8 softmax
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -598,8 +598,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         mbar_arrive_expect_tx(bar(BAR_QFULL + slot), kQBytes);
         tma_load_2d(sQ, &tm_q, bar(BAR_QFULL + slot), xq, d.row0);
         tma_load_2d(sQ + 16384, &tm_q, bar(BAR_QFULL + slot), xq + 64, d.row0);
-        // Load order (the MMA thread consumes in the same order): K0, K1,
-        // then per step j: V_j, K_{j+2}.
+        // Load order (the MMA issuers consume in the same order): K0, K1,
+        // K2, then per step j: V_j, K_{j+3}.
         // kind 0: K (or summary keys), kind 1: V (or summary values)
         auto load = [&](int kind, int step) -> bool {
           const int s = seq % kSlots;
@@ -627,11 +627,10 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           ++seq;
           return true;
         };
-        ok = load(0, 0);
-        if (ok && n > 1) ok = load(0, 1);
+        for (int j = 0; j < 3 && j < n && ok; ++j) ok = load(0, j);
         for (int j = 0; j < n && ok; ++j) {
           ok = load(1, j);
-          if (ok && j + 2 < n) ok = load(0, j + 2);
+          if (ok && j + 3 < n) ok = load(0, j + 3);
           if (*s_abort) ok = false;
         }
         if (ok) mbar_arrive(bar(BAR_UEMPTY + slot));
@@ -645,20 +644,32 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S issuer
+    // S_x = Q K_x^T.  Two threads issue the MMAs (this one S, warp 3's lane 0
+    // PV): one thread's tcgen05.mma issue, not the tensor pipe, limits a
+    // single stream.  Both walk the same ring sequence (K0, K1, K2, then
+    // V_j, K_{j+3} per step) and consume their own kind of slot.
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16(128, 128, false, false);  // S = Q K^T, both K-major
-      const uint32_t id_o = idesc_bf16(128, 128, false, true);   // O += P V, V is MN-major
       // A descriptor's start address is its low 14 bits (16-byte units):
       // stepping through a tile is one add of a compile-time offset.
       auto kmaj_off = [](int kk) { return static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4); };
-      auto vmaj_off = [](int kk) { return static_cast<uint64_t>((kk * 2048) >> 4); };
       auto slot_addr = [&](int q) { return sbase + kOffRing + (q % kSlots) * kSlotBytes; };
       auto wait_full = [&](int q) { return mbar_wait(bar(BAR_FULL + q % kSlots), (q / kSlots) & 1, kWaitLimitNs); };
-      // S_x reuses the buffer of S_{x-2}, which its softmax has read before
-      // releasing P_{x-2}: the PFULL wait of phase x-2 covers it.
-      auto s_col = [&](int gs) { return tmem + kColS + 128u * (gs & 1); };
-      auto p_col = [&](int gs) { return tmem + kColP + 64u * (gs & 1); };
+      // S_x goes to the buffer of S_{x-3}, which holds P_{x-3} until PV_{x-3}
+      // has completed.
+      auto s_col = [&](int gs) { return tmem + kColS + 128u * (gs % 3); };
+      auto buffer_free = [&](int x) {
+        return x < 3 || mbar_wait(bar(BAR_PVDONE + x % 3), ((x - 3) / 3) & 1, kWaitLimitNs);
+      };
+      auto issue_s = [&](int x, uint64_t q_base, int qk) {
+        const uint64_t ks = sdesc_sw128(slot_addr(qk), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ss(s_col(x), q_base + kmaj_off(kk), ks + kmaj_off(kk), id_s, kk > 0 ? 1u : 0u);
+        umma_commit(bar(BAR_EMPTY + qk % kSlots));
+        umma_commit(bar(BAR_SFULL + x % 3));
+      };
       int seq = 0, G = 0;
       bool ok = true;
       for (int k = 0; ok; ++k) {
@@ -669,65 +680,69 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int n = (d.n_ent + 1) / 2;
         if (!mbar_wait(bar(BAR_QFULL + slot), (k >> 1) & 1, kWaitLimitNs)) { ok = false; break; }
         const uint64_t q_base = sdesc_sw128(sbase + kOffQ + slot * kQBytes, 16, 1024);
-        // prologue: S_G (and S_{G+1}), interleaved
-        const int q0 = seq++;
-        const int q1 = n > 1 ? seq++ : -1;
-        ok = wait_full(q0) && (q1 < 0 || wait_full(q1));
-        if (!ok) break;
-        tc_fence_after();
-        {
-          const uint64_t k0 = sdesc_sw128(slot_addr(q0), 16, 1024);
-          const uint64_t k1 = q1 >= 0 ? sdesc_sw128(slot_addr(q1), 16, 1024) : 0;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            umma_ss(s_col(G), q_base + kmaj_off(kk), k0 + kmaj_off(kk), id_s, kk > 0 ? 1u : 0u);
-            if (q1 >= 0) umma_ss(s_col(G + 1), q_base + kmaj_off(kk), k1 + kmaj_off(kk), id_s, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(bar(BAR_EMPTY + q0 % kSlots));
-          umma_commit(bar(BAR_SFULL + (G & 1)));
-          if (q1 >= 0) {
-            umma_commit(bar(BAR_EMPTY + q1 % kSlots));
-            umma_commit(bar(BAR_SFULL + ((G + 1) & 1)));
-          }
-          if (n <= 2) umma_commit(bar(BAR_QEMPTY + slot));  // the unit's last S MMA
+        // S_G .. S_{G+2}
+        for (int j = 0; j < 3 && j < n; ++j) {
+          const int qk = seq++;
+          if (!buffer_free(G + j) || !wait_full(qk)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(G + j, q_base, qk);
         }
+        if (!ok) break;
+        if (n <= 3) umma_commit(bar(BAR_QEMPTY + slot));  // the unit's last S MMA
+        for (int j = 0; j < n && ok; ++j) {
+          ++seq;  // V_j: the PV issuer's slot
+          if (j + 3 >= n) continue;
+          const int qk = seq++;
+          if (!buffer_free(G + j + 3) || !wait_full(qk)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(G + j + 3, q_base, qk);
+          if (j + 3 == n - 1) umma_commit(bar(BAR_QEMPTY + slot));  // the unit's last S MMA
+          if (*s_abort) { ok = false; break; }
+        }
+        if (!ok) break;
+        mbar_arrive(bar(BAR_UEMPTY + slot));
+        G += n;
+      }
+      if (!ok) {
+        *s_abort = 1;
+        set_status(a.status, 5 /* SA_ETIMEOUT */);
+        umma_commit(bar(BAR_DRAIN));
+        mbar_wait(bar(BAR_DRAIN), 0, kWaitLimitNs);
+      }
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ PV issuer
+    if (lane == 0) {
+      const uint32_t id_o = idesc_bf16(128, 128, false, true);  // O += P V, V is MN-major
+      auto vmaj_off = [](int kk) { return static_cast<uint64_t>((kk * 2048) >> 4); };
+      auto slot_addr = [&](int q) { return sbase + kOffRing + (q % kSlots) * kSlotBytes; };
+      auto wait_full = [&](int q) { return mbar_wait(bar(BAR_FULL + q % kSlots), (q / kSlots) & 1, kWaitLimitNs); };
+      auto p_col = [&](int gs) { return tmem + kColS + 128u * (gs % 3); };
+      int seq = 0, G = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int slot = k & 1;
+        if (!wait_unit(k)) { ok = false; break; }
+        const UnitDesc d = udesc[slot];
+        if (!d.valid) break;
+        const int n = (d.n_ent + 1) / 2;
+        seq += n < 3 ? n : 3;  // K0 .. K2: the S issuer's slots
         for (int j = 0; j < n && ok; ++j) {
           const int gs = G + j;
           const int qv = seq++;
-          const bool has_k = j + 2 < n;
-          const int qk = has_k ? seq++ : -1;
+          if (j + 3 < n) ++seq;  // K_{j+3}
           if (!wait_full(qv)) { ok = false; break; }
-          if (!mbar_wait(bar(BAR_PFULL + (gs & 1)), (gs >> 1) & 1, kWaitLimitNs)) { ok = false; break; }
+          if (!mbar_wait(bar(BAR_PFULL + gs % 3), (gs / 3) & 1, kWaitLimitNs)) { ok = false; break; }
           // The unit's first PV overwrites O: the previous epilogue must be done.
           if (j == 0 && k >= 1 && !mbar_wait(bar(BAR_OEMPTY), (k - 1) & 1, kWaitLimitNs)) { ok = false; break; }
           tc_fence_after();
           const uint64_t vs = sdesc_sw128(slot_addr(qv), 16384, 1024);
           const uint32_t pcol = p_col(gs);
-          if (has_k) {
-            if (!wait_full(qk)) { ok = false; break; }
-            tc_fence_after();
-            const uint64_t ks = sdesc_sw128(slot_addr(qk), 16, 1024);
-            const uint32_t scol = s_col(gs + 2);
-            // PV_g and S_{g+2} alternate K-steps: two accumulators in flight.
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              umma_ts(tmem + kColO, pcol + kk * 8, vs + vmaj_off(kk), id_o, (j > 0 || kk > 0) ? 1u : 0u);
-              umma_ss(scol, q_base + kmaj_off(kk), ks + kmaj_off(kk), id_s, kk > 0 ? 1u : 0u);
-            }
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              umma_ts(tmem + kColO, pcol + kk * 8, vs + vmaj_off(kk), id_o, (j > 0 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts(tmem + kColO, pcol + kk * 8, vs + vmaj_off(kk), id_o, (j > 0 || kk > 0) ? 1u : 0u);
           umma_commit(bar(BAR_EMPTY + qv % kSlots));
-          // The softmax of step g waits for PV_{g-1} only to rescale O; for
-          // g < n-1 the commit of S_{g+1} (after PV_{g-1}) already says so.
-          if (j == n - 2) umma_commit(bar(BAR_PVDONE));
-          if (has_k) {
-            umma_commit(bar(BAR_EMPTY + qk % kSlots));
-            umma_commit(bar(BAR_SFULL + (gs & 1)));
-            if (j + 2 == n - 1) umma_commit(bar(BAR_QEMPTY + slot));  // the unit's last S MMA
-          }
+          umma_commit(bar(BAR_PVDONE + gs % 3));
           if (*s_abort) { ok = false; break; }
         }
         if (!ok) break;
@@ -738,8 +753,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (!ok) {
         *s_abort = 1;
         set_status(a.status, 5 /* SA_ETIMEOUT */);
-        umma_commit(bar(BAR_DRAIN));
-        mbar_wait(bar(BAR_DRAIN), 0, kWaitLimitNs);
+        umma_commit(bar(BAR_DRAIN2));
+        mbar_wait(bar(BAR_DRAIN2), 0, kWaitLimitNs);
       }
     }
   } else if (warp >= 4) {
@@ -754,7 +769,6 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     float* rref = xchg;                    // [3][128]: reference after step g at g % 3
     float* xl = xchg + 3 * 128;            // [2][128]: partial row sums
     int G = 0;
-    int pv_units = 0;  // units of n >= 2 steps before this one (PV-done commits)
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int slot = k & 1;
@@ -772,8 +786,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       for (int j = ((G & 1) == grp) ? 0 : 1; j < n && ok; j += 2) {
         const int gs = G + j;
         const int b = gs % 3;        // reference slot
-        const int sb = gs & 1;       // S and P buffers
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_SFULL + sb), (gs >> 1) & 1, kWaitLimitNs));
+        const int sb = gs % 3;       // S buffer (P_g goes over S_g's first 64 columns)
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_SFULL + sb), (gs / 3) & 1, kWaitLimitNs));
         if (!ok) break;
         tc_fence_after();
         const uint32_t scol = tmem + lane_addr + kColS + 128u * sb;
@@ -853,8 +867,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           my_ref = ref;
         }
         const float msub = (ref == -INFINITY) ? 0.f : ref;
-        // P_g goes where P_{g-2} was: PV_{g-2} has completed, since S_g was
-        // committed after it.
+        // P_g goes over S_g's first 64 columns, after both passes have read
+        // them (half 0's P after half 0's reads).
         uint64_t acc[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[q] = f2(0.f, 0.f);
@@ -904,8 +918,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
           }
           // P (BF16 pairs) of this half into columns [32 hh, 32 hh + 32) of
-          // P_g's buffer.
-          tmem_st32(tmem + lane_addr + kColP + 64u * sb + 32u * hh, p);
+          // S_g's buffer: columns already consumed by both passes of half 0.
+          tmem_st32(tmem + lane_addr + kColS + 128u * sb + 32u * hh, p);
         }
         {
           float a0, a1, b0, b1, c0, c1, d0, d1;
@@ -917,15 +931,11 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         tmem_wait_st();
         // O holds sum_{i<g} P_i V_i relative to `prev`; move it to `ref`
-        // before P_g is released to the MMA thread.
+        // before P_g is released to the PV issuer.
         if (__any_sync(0xFFFFFFFFu, resc)) {
-          // PV_{g-1} must have finished before O is rescaled (j >= 1 here):
-          // S_{g+1} was committed after it, or, for the unit's last step, the
-          // unit's PV-done commit (step n-2) says so.
-          const bool via_s = j + 1 < n;
-          const uint32_t wb = via_s ? bar(BAR_SFULL + ((gs + 1) & 1)) : bar(BAR_PVDONE);
-          const uint32_t wp = via_s ? (((gs + 1) >> 1) & 1) : static_cast<uint32_t>(pv_units & 1);
-          if (!__all_sync(0xFFFFFFFFu, mbar_wait(wb, wp, kWaitLimitNs))) {
+          // PV_{g-1} must have finished before O is rescaled (j >= 1 here).
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_PVDONE + (gs - 1) % 3), ((gs - 1) / 3) & 1,
+                                                 kWaitLimitNs))) {
             ok = false;
             break;
           }
@@ -1005,7 +1015,6 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       }
       ok = !named_bar_or(2, kSoftmaxThreads, *s_abort != 0);
       G += n;
-      if (n >= 2) ++pv_units;
     }
     if (!ok) {
       *s_abort = 1;
