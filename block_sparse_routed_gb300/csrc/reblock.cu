@@ -68,8 +68,8 @@ __host__ __device__ __forceinline__ int pow2_children(int m, int fanout) {
 }
 
 // Node of tree depth `level` that holds block x (blocks of 64 tokens,
-// numbered in the final order's span): its first block and block count.
-// `leaf` when the walk met a finished leaf before that depth.
+// numbered in the final order's span): its first block and block count, or
+// the leaf (one block) that holds x when the tree ends above that depth.
 __device__ __forceinline__ void find_node(int x, int m_root, int fanout, int level, int& start, int& m,
                                           bool& leaf) {
   start = 0;
@@ -186,10 +186,9 @@ __device__ __forceinline__ int node_blocks(int x, int m_root, int fanout, int le
 }
 
 // Farthest landmark pair of every split node of the level: CTA (k, h).  The
-// landmarks' unit rows go to shared memory (rows padded to 129 floats so a
-// warp reading different rows hits different banks); each thread takes Gram
-// entries in increasing pair number (pairs numbered in (j, j') order) and
-// keeps the smallest cosine with a strict <, so ties go to the lower pair.
+// landmarks' unit rows go to shared memory; each thread takes Gram entries
+// in increasing pair number (pairs numbered in (j, j') order) and keeps the
+// smallest cosine with a strict <, so ties go to the lower pair.
 __global__ void __launch_bounds__(kPairThreads) reblock_pair_kernel(const __half* __restrict__ xh,
                                                                    const int32_t* __restrict__ ord,
                                                                    int2* __restrict__ pairs, int N, int fanout,
