@@ -222,3 +222,18 @@ def test_fold_order_and_fp16_units():
     assert np.max(np.abs(u - ref)) <= 2.0 ** -11
     assert np.allclose(np.linalg.norm(u, axis=1), 1.0, atol=2e-3)
     assert np.array_equal(u.astype(np.float16).astype(np.float32), u)
+
+
+def test_tree_depth_used_for_launch_counts_matches_the_recursion():
+    # bench.py counts 3 launches per tree level; its depth must be the depth
+    # of the recursion the oracle runs (not monotone in m: fanout 8 splits 8
+    # blocks in one level, 7 blocks in two)
+    import bench
+
+    def depth(m, f):
+        return 0 if m == 1 else 1 + max(depth(s, f) for s in R.child_blocks(m, f))
+
+    for f in (2, 4, 8, 16):
+        for m in range(1, 400):
+            assert bench.reblock_depth(m, f) == depth(m, f), (m, f)
+    assert bench.reblock_depth(148, 8) == 4  # the H3 keys: 148 blocks
