@@ -37,6 +37,7 @@ ENTRY_POINTS = (
     "sparse_attn_reblock_ws_bytes",
     "sparse_attn_spark_reblock",
     "sparse_attn_last_device_status",
+    "sparse_attn_set_single_probe_waits",
     "sparse_attn_last_cuda_error",
     "sparse_attn_status_string",
 )
@@ -131,6 +132,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.sparse_attn_fwd.restype = ctypes.c_int
     lib.sparse_attn_last_device_status.argtypes = [vp, vp, P(ctypes.c_int)]
     lib.sparse_attn_last_device_status.restype = ctypes.c_int
+    lib.sparse_attn_set_single_probe_waits.argtypes = [ctypes.c_int]
+    lib.sparse_attn_set_single_probe_waits.restype = ctypes.c_int
     lib.sparse_attn_last_cuda_error.argtypes = [P(ctypes.c_char_p)]
     lib.sparse_attn_last_cuda_error.restype = ctypes.c_int
     lib.sparse_attn_spark_reweight.argtypes = [P(SaReweightParams), vp, vp, vp, vp, vp, vp, vp]
@@ -246,6 +249,13 @@ def sparse_attn_last_device_status(ws, stream) -> int:
     if st != SA_OK:
         raise SparseAttnError(st, "sparse_attn_last_device_status")
     return out.value
+
+
+def sparse_attn_set_single_probe_waits(on: bool) -> int:
+    """Testing hook: later attention launches use the kernel build whose
+    pipeline waits are single probes (to exercise the timeout path).  Returns
+    the previous setting."""
+    return int(load_library().sparse_attn_set_single_probe_waits(1 if on else 0))
 
 
 def sparse_attn_last_cuda_error():

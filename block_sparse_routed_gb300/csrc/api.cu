@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -15,16 +16,21 @@
 #define SA_API extern "C" __attribute__((visibility("default")))
 
 namespace {
-using namespace sa;
-
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+}  // namespace
 
-// Records a failed CUDA call for sparse_attn_last_cuda_error.
-bool cuda_failed(cudaError_t e) {
+bool sa::cuda_failed(cudaError_t e) {
   if (e == cudaSuccess) return false;
   g_last_cuda_error = e;
   return true;
 }
+
+namespace {
+using namespace sa;
+
+// Testing hook: launch the attention kernel's single-probe-wait build (see
+// sparse_attn_set_single_probe_waits).
+std::atomic<int> g_probe_once{0};
 
 constexpr uint64_t align256(uint64_t x) { return (x + 255u) & ~uint64_t(255); }
 
@@ -252,6 +258,7 @@ SA_API sa_status sparse_attn_fwd(const sa_params* p, const void* q, const void* 
   a.fused = 0;
   a.qc = a.kc = nullptr;
   a.idx_w = a.cnt_w = nullptr;
+  a.probe_once = g_probe_once.load();
   // the summary maps are unused without merging
   if (cuda_failed(launch_attention(tq, tk, tv, tk, tv, a, stream))) return SA_ECUDA;
   return SA_OK;
@@ -342,6 +349,7 @@ SA_API sa_status sparse_attn_fused(const sa_params* p, const void* q, const void
   a.kc = pa.kc;
   a.idx_w = idx;
   a.cnt_w = cnt;
+  a.probe_once = g_probe_once.load();
   if (cuda_failed(launch_attention(tq, tk, tv, tk, tv, a, stream))) return SA_ECUDA;
   return SA_OK;
 }
@@ -429,6 +437,7 @@ SA_API sa_status sparse_attn_spark_fwd(const sa_params* p, const void* q, const 
   a.fused = 0;
   a.qc = a.kc = nullptr;
   a.idx_w = a.cnt_w = nullptr;
+  a.probe_once = g_probe_once.load();
   if (cuda_failed(launch_attention(tq, tk, tv, tak, tav, a, stream))) return SA_ECUDA;
   return SA_OK;
 }
@@ -522,6 +531,8 @@ SA_API sa_status sparse_attn_last_device_status(const void* ws, cudaStream_t str
   *out = static_cast<sa_status>(v);
   return SA_OK;
 }
+
+SA_API int sparse_attn_set_single_probe_waits(int on) { return g_probe_once.exchange(on ? 1 : 0); }
 
 SA_API int sparse_attn_last_cuda_error(const char** message) {
   const cudaError_t e = g_last_cuda_error;

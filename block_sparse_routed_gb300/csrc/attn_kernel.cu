@@ -239,7 +239,9 @@ __device__ __forceinline__ void decode_unit(const AttnArgs& a, int u, UnitDesc& 
 // block means) instead of reading the plan's lists, and exports the lists.
 // Each mode is its own instantiation so that the exact path's softmax code
 // stays as compact as it can be.
-template <bool kMerged, bool kFused>
+// kProbeOnce: every pipeline wait is a single probe (a testing build of the
+// kernel that exercises the timeout path; the abort drains keep their limit).
+template <bool kMerged, bool kFused, bool kProbeOnce>
 __global__ void __launch_bounds__(kThreads, 1)
 attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_ak,
@@ -255,6 +257,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   volatile int32_t* s_abort = reinterpret_cast<volatile int32_t*>(base + kOffMisc + 16);
   volatile int32_t* s_status = reinterpret_cast<volatile int32_t*>(base + kOffMisc + 24);
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * i; };
+  constexpr uint64_t lim = kProbeOnce ? 0 : kWaitLimitNs;  // pipeline waits (drains: kWaitLimitNs)
   auto ent_buf = [&](int slot) { return reinterpret_cast<int32_t*>(base + kOffEnt + 4u * kMaxEnt * slot); };
   // keep-masks of the summary keys of a unit: [chunk][row half], bit u set
   // when video block 64 chunk + u is skipped by that half's list
@@ -307,7 +310,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   };
   // Waits for unit k's descriptor; false when waiting failed.
   auto wait_unit = [&](int k) -> bool {
-    return mbar_wait(bar(BAR_UFULL + (k & 1)), (k >> 1) & 1, kWaitLimitNs);
+    return mbar_wait(bar(BAR_UFULL + (k & 1)), (k >> 1) & 1, lim);
   };
 
   // Fused route of a sparse unit (scheduler warp): for query blocks iA and
@@ -452,7 +455,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     for (int k = 0;; ++k) {
       const int slot = k & 1;
       bool ok = true;
-      if (k >= 2) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_UEMPTY + slot), ((k - 2) >> 1) & 1, kWaitLimitNs));
+      if (k >= 2) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_UEMPTY + slot), ((k - 2) >> 1) & 1, lim));
       if (!ok || *s_abort) {
         *s_abort = 1;
         set_status(a.status, 5 /* SA_ETIMEOUT */);
@@ -477,7 +480,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             nA = a.cnt[static_cast<size_t>(d.h) * g.nq + d.iA];
             nB = (d.iB >= 0) ? a.cnt[static_cast<size_t>(d.h) * g.nq + d.iB] : 0;
           }
-          bad = nA < 1 || nA > g.maxl || nB < 0 || nB > g.maxl;
+          bad = nA < 1 || nA > g.maxl || (d.iB >= 0 && (nB < 1 || nB > g.maxl));
           if (!bad) {
             if constexpr (!kFused) {
               const int32_t* ga = a.idx + (static_cast<size_t>(d.h) * g.nq + d.iA) * g.maxl;
@@ -593,7 +596,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (!d.valid) break;
         const int n = (d.n_ent + 1) / 2;
         const int xq = d.h * kHeadDim;
-        if (k >= 2 && !mbar_wait(bar(BAR_QEMPTY + slot), ((k - 2) >> 1) & 1, kWaitLimitNs)) { ok = false; break; }
+        if (k >= 2 && !mbar_wait(bar(BAR_QEMPTY + slot), ((k - 2) >> 1) & 1, lim)) { ok = false; break; }
         const uint32_t sQ = sbase + kOffQ + slot * kQBytes;
         mbar_arrive_expect_tx(bar(BAR_QFULL + slot), kQBytes);
         tma_load_2d(sQ, &tm_q, bar(BAR_QFULL + slot), xq, d.row0);
@@ -604,7 +607,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         auto load = [&](int kind, int step) -> bool {
           const int s = seq % kSlots;
           const uint32_t par = ((seq / kSlots) & 1) ^ 1;
-          if (!mbar_wait(bar(BAR_EMPTY + s), par, kWaitLimitNs)) return false;
+          if (!mbar_wait(bar(BAR_EMPTY + s), par, lim)) return false;
           const uint32_t dst = sbase + kOffRing + s * kSlotBytes;
           mbar_arrive_expect_tx(bar(BAR_FULL + s), kSlotBytes);
 #pragma unroll
@@ -655,12 +658,12 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       // stepping through a tile is one add of a compile-time offset.
       auto kmaj_off = [](int kk) { return static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4); };
       auto slot_addr = [&](int q) { return sbase + kOffRing + (q % kSlots) * kSlotBytes; };
-      auto wait_full = [&](int q) { return mbar_wait(bar(BAR_FULL + q % kSlots), (q / kSlots) & 1, kWaitLimitNs); };
+      auto wait_full = [&](int q) { return mbar_wait(bar(BAR_FULL + q % kSlots), (q / kSlots) & 1, lim); };
       // S_x goes to the buffer of S_{x-3}, which holds P_{x-3} until PV_{x-3}
       // has completed.
       auto s_col = [&](int gs) { return tmem + kColS + 128u * (gs % 3); };
       auto buffer_free = [&](int x) {
-        return x < 3 || mbar_wait(bar(BAR_PVDONE + x % 3), ((x - 3) / 3) & 1, kWaitLimitNs);
+        return x < 3 || mbar_wait(bar(BAR_PVDONE + x % 3), ((x - 3) / 3) & 1, lim);
       };
       auto issue_s = [&](int x, uint64_t q_base, int qk) {
         const uint64_t ks = sdesc_sw128(slot_addr(qk), 16, 1024);
@@ -678,7 +681,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const UnitDesc d = udesc[slot];
         if (!d.valid) break;
         const int n = (d.n_ent + 1) / 2;
-        if (!mbar_wait(bar(BAR_QFULL + slot), (k >> 1) & 1, kWaitLimitNs)) { ok = false; break; }
+        if (!mbar_wait(bar(BAR_QFULL + slot), (k >> 1) & 1, lim)) { ok = false; break; }
         const uint64_t q_base = sdesc_sw128(sbase + kOffQ + slot * kQBytes, 16, 1024);
         // S_G .. S_{G+2}
         for (int j = 0; j < 3 && j < n; ++j) {
@@ -716,7 +719,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       const uint32_t id_o = idesc_bf16(128, 128, false, true);  // O += P V, V is MN-major
       auto vmaj_off = [](int kk) { return static_cast<uint64_t>((kk * 2048) >> 4); };
       auto slot_addr = [&](int q) { return sbase + kOffRing + (q % kSlots) * kSlotBytes; };
-      auto wait_full = [&](int q) { return mbar_wait(bar(BAR_FULL + q % kSlots), (q / kSlots) & 1, kWaitLimitNs); };
+      auto wait_full = [&](int q) { return mbar_wait(bar(BAR_FULL + q % kSlots), (q / kSlots) & 1, lim); };
       auto p_col = [&](int gs) { return tmem + kColS + 128u * (gs % 3); };
       int seq = 0, G = 0;
       bool ok = true;
@@ -732,9 +735,9 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           const int qv = seq++;
           if (j + 3 < n) ++seq;  // K_{j+3}
           if (!wait_full(qv)) { ok = false; break; }
-          if (!mbar_wait(bar(BAR_PFULL + gs % 3), (gs / 3) & 1, kWaitLimitNs)) { ok = false; break; }
+          if (!mbar_wait(bar(BAR_PFULL + gs % 3), (gs / 3) & 1, lim)) { ok = false; break; }
           // The unit's first PV overwrites O: the previous epilogue must be done.
-          if (j == 0 && k >= 1 && !mbar_wait(bar(BAR_OEMPTY), (k - 1) & 1, kWaitLimitNs)) { ok = false; break; }
+          if (j == 0 && k >= 1 && !mbar_wait(bar(BAR_OEMPTY), (k - 1) & 1, lim)) { ok = false; break; }
           tc_fence_after();
           const uint64_t vs = sdesc_sw128(slot_addr(qv), 16384, 1024);
           const uint32_t pcol = p_col(gs);
@@ -769,10 +772,13 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     float* rref = xchg;                    // [3][128]: reference after step g at g % 3
     float* xl = xchg + 3 * 128;            // [2][128]: partial row sums
     int G = 0;
-    bool ok = true;
+    // All 256 softmax threads agree on entering each unit (its descriptor
+    // arrived for every warp): a warp whose wait gave up must not leave the
+    // others at the group barriers.  The agreement for unit k + 1 rides on
+    // the barrier that ends unit k.
+    bool ok = !named_bar_or(2, kSoftmaxThreads, !__all_sync(0xFFFFFFFFu, wait_unit(0)) || *s_abort != 0);
     for (int k = 0; ok; ++k) {
       const int slot = k & 1;
-      if (!__all_sync(0xFFFFFFFFu, wait_unit(k))) { ok = false; break; }
       const UnitDesc d = udesc[slot];
       if (!d.valid) break;
       const int n = (d.n_ent + 1) / 2;
@@ -787,7 +793,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int gs = G + j;
         const int b = gs % 3;        // reference slot
         const int sb = gs % 3;       // S buffer (P_g goes over S_g's first 64 columns)
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_SFULL + sb), (gs / 3) & 1, kWaitLimitNs));
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_SFULL + sb), (gs / 3) & 1, lim));
         if (!ok) break;
         tc_fence_after();
         const uint32_t scol = tmem + lane_addr + kColS + 128u * sb;
@@ -850,7 +856,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // reference after step g-1 of this unit (published by the other group)
         if (j > 0) {
           if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_MREADY + (gs - 1) % 3), ((gs - 1) / 3) & 1,
-                                                 kWaitLimitNs))) {
+                                                 lim))) {
             ok = false;
             break;
           }
@@ -935,7 +941,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (__any_sync(0xFFFFFFFFu, resc)) {
           // PV_{g-1} must have finished before O is rescaled (j >= 1 here).
           if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_PVDONE + (gs - 1) % 3), ((gs - 1) / 3) & 1,
-                                                 kWaitLimitNs))) {
+                                                 lim))) {
             ok = false;
             break;
           }
@@ -958,10 +964,10 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (__any_sync(0xFFFFFFFFu, *s_abort != 0)) ok = false;
       }
       // ---- epilogue of the unit
-      ok = ok && __all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_OFULL), k & 1, kWaitLimitNs));
+      ok = ok && __all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_OFULL), k & 1, lim));
       const int last = G + n - 1;
       if (ok && (last & 1) != grp)  // the other group published the last reference
-        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_MREADY + last % 3), (last / 3) & 1, kWaitLimitNs));
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_MREADY + last % 3), (last / 3) & 1, lim));
       float fin = -INFINITY;
       if (ok) {
         tc_fence_after();
@@ -1013,7 +1019,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         mbar_arrive(bar(BAR_OEMPTY));
         mbar_arrive(bar(BAR_UEMPTY + slot));
       }
-      ok = !named_bar_or(2, kSoftmaxThreads, *s_abort != 0);
+      const bool got = __all_sync(0xFFFFFFFFu, wait_unit(k + 1));
+      ok = !named_bar_or(2, kSoftmaxThreads, !got || *s_abort != 0);
       G += n;
     }
     if (!ok) {
@@ -1071,16 +1078,18 @@ cudaError_t launch_bias_prep(const float* bias, float* b2, int32_t* status, cons
 cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                              const CUtensorMap& tak, const CUtensorMap& tav, const AttnArgs& a,
                              cudaStream_t s) {
-  auto* kern = a.merged ? attention_kernel<true, false>
-                        : (a.fused ? attention_kernel<false, true> : attention_kernel<false, false>);
+  const bool probe = a.probe_once != 0;
+  auto* kern = a.merged ? (probe ? attention_kernel<true, false, true> : attention_kernel<true, false, false>)
+                        : (a.fused ? (probe ? attention_kernel<false, true, true> : attention_kernel<false, true, false>)
+                                   : (probe ? attention_kernel<false, false, true> : attention_kernel<false, false, false>));
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
   if (e != cudaSuccess) return e;
   // The register split redistributes the block's launch allocation; a build
   // that allocated fewer registers per thread would make setmaxnreg.inc wait
   // forever, so refuse to launch it.
-  static int regs[3] = {-1, -1, -1};
-  int& rg = regs[a.merged ? 1 : (a.fused ? 2 : 0)];
+  static int regs[6] = {-1, -1, -1, -1, -1, -1};
+  int& rg = regs[(a.merged ? 1 : (a.fused ? 2 : 0)) + (probe ? 3 : 0)];
   if (rg < 0) {
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, kern);

@@ -64,6 +64,7 @@ struct AttnArgs {
   const float* kc;     // [H, nvk, 128]
   int32_t* idx_w;
   int32_t* cnt_w;
+  int probe_once;      // testing build: every pipeline wait is a single probe
 };
 
 constexpr int kMaxFusedVideoBlocks = 256;  // video key blocks a fused route supports
@@ -79,6 +80,10 @@ struct ReweightArgs {
   float* lm;           // [P, H, nblk]
   int T, H, P, nblk;
 };
+
+// Records a failed CUDA call for sparse_attn_last_cuda_error (thread-local,
+// defined in api.cu); returns true when `e` is an error.
+bool cuda_failed(cudaError_t e);
 
 // Launchers (defined in the kernel translation units).
 cudaError_t launch_pool(const PlanArgs& a, cudaStream_t s);

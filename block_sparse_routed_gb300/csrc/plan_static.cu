@@ -14,10 +14,13 @@
 // the GPU (other streams, other host threads) race; the caller serialises
 // them.  The host cannot use the array's name as a device address: the first
 // call on each device looks the address up with cudaGetSymbolAddress while
-// that device is current, and caches it.  That first call should come before
-// any stream capture.
+// that device is current, and caches it with its context (a new context, as
+// after a device reset, is looked up again).  That first call should come
+// before any stream capture.
 #include <cstdint>
 #include <mutex>
+
+#include <cudaTypedefs.h>
 
 #include "internal.h"
 #include "sparse_attn.h"
@@ -33,30 +36,54 @@ constexpr int kMaxDevices = 128;
 
 uint64_t align256(uint64_t x) { return (x + 255u) & ~uint64_t(255); }
 
-// Per-device set-up: sm_103 check and the device address of g_plan_scratch.
+PFN_cuCtxGetCurrent_v4000 ctx_get_current() {
+  static std::once_flag once;
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+  });
+  return fn;
+}
+
+// Set-up per device and context: the sm_103 check and the device address of
+// g_plan_scratch, looked up with that device current.  The address is
+// cached per device together with the context it was resolved in; when the
+// current context is another one (say the device was reset and its primary
+// context created again, which loads the module again), it is looked up
+// again.  cuCtxGetCurrent is cheap and allowed during stream capture.
 sa_status scratch_for_current_device(uint8_t** out) {
   static std::mutex mu;
   static uint8_t* addr[kMaxDevices] = {nullptr};
-  static signed char state[kMaxDevices] = {0};  // 0 not set up, 1 ready, -1 unsupported
+  static CUcontext ctx_of[kMaxDevices] = {nullptr};
+  static signed char state[kMaxDevices] = {0};  // 0 not checked, 1 sm_103, -1 unsupported
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SA_ECUDA;
+  if (cuda_failed(cudaGetDevice(&dev))) return SA_ECUDA;
   if (dev < 0 || dev >= kMaxDevices) return SA_EUNSUPPORTED;
+  auto get_ctx = ctx_get_current();
+  if (!get_ctx) return SA_ECUDA;
   std::lock_guard<std::mutex> lock(mu);
   if (state[dev] == 0) {
     int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    if (cuda_failed(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) ||
+        cuda_failed(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)))
       return SA_ECUDA;
-    if (!(major == 10 && minor == 3)) {
-      state[dev] = -1;
-    } else {
-      void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_plan_scratch) != cudaSuccess || p == nullptr) return SA_ECUDA;
-      addr[dev] = static_cast<uint8_t*>(p);
-      state[dev] = 1;
-    }
+    state[dev] = (major == 10 && minor == 3) ? 1 : -1;
   }
   if (state[dev] != 1) return SA_EUNSUPPORTED;
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return SA_ECUDA;
+  if (ctx == nullptr || ctx != ctx_of[dev] || addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cuda_failed(cudaGetSymbolAddress(&p, g_plan_scratch))) return SA_ECUDA;
+    if (p == nullptr) return SA_ECUDA;
+    if (get_ctx(&ctx) != CUDA_SUCCESS) return SA_ECUDA;  // the runtime may have made the context
+    addr[dev] = static_cast<uint8_t*>(p);
+    ctx_of[dev] = ctx;
+  }
   *out = addr[dev];
   return SA_OK;
 }
@@ -108,8 +135,8 @@ SA_API sa_status sparse_attn_plan_static(const sa_params* p, const void* q, cons
   a.g = g;
   // The status area must start at zero on every call; the means are fully
   // overwritten by the pooling kernel.
-  if (cudaMemsetAsync(scratch, 0, kStatusBytes, stream) != cudaSuccess) return SA_ECUDA;
-  if (launch_pool(a, stream) != cudaSuccess) return SA_ECUDA;
-  if (launch_route_topk(a, stream) != cudaSuccess) return SA_ECUDA;
+  if (cuda_failed(cudaMemsetAsync(scratch, 0, kStatusBytes, stream))) return SA_ECUDA;
+  if (cuda_failed(launch_pool(a, stream))) return SA_ECUDA;
+  if (cuda_failed(launch_route_topk(a, stream))) return SA_ECUDA;
   return SA_OK;
 }

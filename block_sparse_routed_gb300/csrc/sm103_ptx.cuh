@@ -67,9 +67,10 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 
 // Waits for the phase with the given parity to complete.  Gives up after
 // `limit_ns` nanoseconds of wall time and returns false, so that a lost
-// arrival can never hang the GPU.
+// arrival can never hang the GPU.  limit_ns = 0 is a single probe.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_test_wait(bar, parity)) return true;
+  if (limit_ns == 0) return false;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1

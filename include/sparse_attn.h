@@ -132,7 +132,10 @@ sa_status sparse_attn_plan(const sa_params* p, const void* q, const void* k, int
  *             u < 64 nvk (else SA_ENOSINKBIAS); NaN or +inf anywhere gives
  *             SA_EINVAL; -inf removes the key.  Both are device-detected:
  *             read them with sparse_attn_last_device_status.
- *   idx, cnt  block lists from sparse_attn_plan (same params)
+ *   idx, cnt  block lists from sparse_attn_plan (same params).  Lists are
+ *             checked on the device before any of their blocks is loaded:
+ *             1 <= cnt <= maxl, entries in [0, nblk) and strictly increasing,
+ *             else SA_EINVAL (device-detected)
  *   o         BF16 [1, T, H, 128]; every row is written when the device
  *             status is SA_OK
  *   ws        workspace of at least fwd_ws_bytes (may alias none of the
@@ -312,6 +315,20 @@ sa_status sparse_attn_spark_reblock(const sa_reblock_params* p, const void* x, i
  * enqueued with it).  Synchronises `stream`.  SA_ECUDA if the copy fails.
  */
 sa_status sparse_attn_last_device_status(const void* ws, cudaStream_t stream, sa_status* out);
+
+/*
+ * Testing hook (the source pages have no counterpart).  Every on-device
+ * pipeline wait of the attention kernels gives up after 1 s: the kernel then
+ * records SA_ETIMEOUT in the workspace status word, lets its own copies and
+ * MMAs in flight finish (those waits keep the 1 s limit), frees its tensor
+ * memory and returns; the outputs of that call are invalid.  With `on`
+ * nonzero, later launches by sparse_attn_fwd, sparse_attn_spark_fwd and
+ * sparse_attn_fused use a build of the kernel in which every pipeline wait
+ * is a single probe, so that a call almost surely times out: it exists to
+ * test that path.  Process-wide; returns the previous setting (0 or 1).
+ * Host only: touches no device.
+ */
+int sparse_attn_set_single_probe_waits(int on);
 
 /*
  * The last CUDA runtime error that made an entry point return SA_ECUDA on

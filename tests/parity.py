@@ -82,3 +82,57 @@ def bf16_tensor_to_f64(t):
 def output_errors(o_gpu, o_ref):
     d = np.abs(o_gpu - o_ref)
     return float(d.max()), float(d.mean())
+
+
+# ---------------------------------------------------------------- oracle outputs, every head
+def _oracle_head(args):
+    """One head of the oracle's output (runs in a spawned worker)."""
+    kind, qh, kh, vh, bias, idx_h, cnt_h, prm = args
+    import oracle as O
+
+    sz = O.derive_sizes(prm["T"], 1, prm["video_tokens"], prm["topk_ratio"], prm["radius"], prm["tail_mode"])
+    if kind == "exact":
+        return O.forward(qh, kh, vh, bias, idx_h, cnt_h, sz)[:, 0]
+    a = O.video_query_anchor(qh, sz.Nv)
+    s = O.spark_reweight(a, kh, vh)
+    return O.forward_merged(qh, kh, vh, bias, idx_h, cnt_h, sz, s["ak16"][0], s["av16"][0], s["lm"][0])[:, 0]
+
+
+def oracle_pool(max_workers=16):
+    """A spawned process pool for the oracle (safe after CUDA is initialised),
+    one BLAS thread per worker."""
+    import multiprocessing as mp
+    import os
+
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ.setdefault(var, "1")
+    n = max(1, min(max_workers, len(os.sched_getaffinity(0))))
+    return mp.get_context("spawn").Pool(n)
+
+
+def oracle_all_heads(pool, kind, arrays, prm, idx, cnt):
+    """The oracle's output for every head, O [T, H, 128] fp64, with the
+    oracle's own lists; kind is "exact" (oracle.forward) or "merged"
+    (oracle.spark: anchor, summaries, forward_merged)."""
+    H = idx.shape[0]
+    tasks = [(kind, np.ascontiguousarray(arrays["q"][:, [h]]), np.ascontiguousarray(arrays["k"][:, [h]]),
+              np.ascontiguousarray(arrays["v"][:, [h]]), arrays["bias"], idx[[h]], cnt[[h]], prm)
+             for h in range(H)]
+    outs = pool.map(_oracle_head, tasks, chunksize=1)
+    return np.stack(outs, axis=1)
+
+
+def compare_all(o_gpu, o_ref, same, sz):
+    """max and mean |O_gpu - O_oracle| over every (row, head, dim) except the
+    rows of query blocks whose GPU list differs from the oracle's (near-tie
+    rule); also the number of values compared."""
+    import oracle as O
+
+    keep = np.ones(o_gpu.shape[:2], dtype=bool)
+    for h in range(same.shape[0]):
+        for i in range(same.shape[1]):
+            if not same[h, i]:
+                r = O.oracle.query_block_rows(i, sz)
+                keep[r.start:r.stop, h] = False
+    d = np.abs(o_gpu - o_ref)[keep]
+    return float(d.max()), float(d.mean()), int(d.size)

@@ -244,3 +244,14 @@ def test_reblock_rejects_bad_arguments_before_launch(native):
     up = lambda b: (b + 255) // 256 * 256
     assert need == up(960 * 2 * 256) + up(960 * 2 * 8) + 2 * up(960 * 2 * 4) + up(15 * 2 * 8)
     assert ws_bytes(params(T=40)) == (native.SA_OK, 0)
+
+
+def test_single_probe_hook_round_trips_on_the_host(native):
+    # host-only setter: returns the previous setting, touches no device
+    prev = native.sparse_attn_set_single_probe_waits(True)
+    try:
+        assert prev == 0  # off by default
+        assert native.sparse_attn_set_single_probe_waits(False) == 1
+    finally:
+        native.sparse_attn_set_single_probe_waits(bool(prev))
+    assert native.sparse_attn_set_single_probe_waits(False) == 0
