@@ -1,16 +1,18 @@
 """Benchmark: Top-K block-sparse routed attention, plan + fwd, on one GB300.
 
 A step is one pass of the whole path (pool, route + Top-K + lists, attention
-over the lists, dense rows) over the H3-shaped workload: 9505 packed tokens
-(9240 video + 265 context), 56 heads, head dim 128, BF16, Top-K ratio 0.1,
-radius 1, dense tail.  Inputs are synthetic (block-clustered random walks,
-seeded) and resident in HBM; Q + K + V + O = 545 MB is larger than the 126 MB
-L2, so no flush is needed between steps.
+over the lists, dense rows) over one workload, by default the H3-shaped one:
+9505 packed tokens (9240 video + 265 context), 56 heads, head dim 128, BF16,
+Top-K ratio 0.1, radius 1, dense tail.  Inputs are synthetic (block-clustered
+random walks, seeded) and resident in HBM; Q + K + V + O = 545 MB is larger
+than the 126 MB L2, so no flush is needed between steps (one extra leg times
+the forward with L2 flushed before every call).
 
 The metric is kept-block attention TFLOP/s: 4 * 128 FLOP per (real query
 row, kept key) pair, summed over heads, divided by the step time.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload tiny|8k|h3|32k|64k]
     python bench.py --op reweight      # Spark virtual summaries instead
     python bench.py --op spark         # Spark merged attention (plan + merged fwd)
     python bench.py --op reblock       # Spark token reblocking (landmark tree) of the H3 keys
@@ -20,10 +22,11 @@ virtual summaries (sparse_attn_spark_reweight) over the same H3-shaped K/V
 with one anchor per head: HBM bytes per second against the measured copy
 bandwidth (K and V read once; summaries written).
 
-Rank 0 prints one JSON line.  With N > 1 (torchrun), every rank runs its own
-independent copy of the workload (weak scaling: heads and problems are
-independent, no collective in the data path); the timing is the max over
-ranks.  ``--impl reference`` times the CPU fp64 oracle on the host cores.
+Rank 0 prints one JSON line.  With N > 1 (torchrun), the heads are split
+into N contiguous slices, one per rank (heads are independent: no collective
+in the data path), so the job does the workload once ("scaling": "strong");
+the timing is the max over ranks.  ``--impl reference`` times the CPU fp64
+oracle on the host cores.
 """
 
 from __future__ import annotations
@@ -197,9 +200,39 @@ def max_over_ranks(x, world, device):
 
 
 def weak_scaling_value(kept_flop_per_rank, ms_per_step, world):
-    """Whole-job kept TFLOP/s: every rank runs its own copy of the workload,
-    so the job does `world` copies in the slowest rank's step time."""
+    """Whole-job kept TFLOP/s when every rank runs its own copy of the
+    workload: the job does `world` copies in the slowest rank's step time."""
     return world * kept_flop_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
+def head_range(H, rank, world):
+    """The contiguous heads [h0, h1) of `rank` when H heads are split over
+    `world` ranks (sizes differ by at most one, larger slices first)."""
+    base, extra = divmod(H, world)
+    h0 = rank * base + min(rank, extra)
+    return h0, h0 + base + (1 if rank < extra else 0)
+
+
+def split_heads(arrays, h0, h1):
+    """This rank's inputs: the heads [h0, h1) of Q, K, V ([T, H, 128] BF16
+    bits) as contiguous arrays; the key bias is per key and shared."""
+    out = dict(arrays)
+    for n in ("q", "k", "v"):
+        out[n] = np.ascontiguousarray(arrays[n][:, h0:h1])
+    return out
+
+
+def strong_scaling_value(kept_flop_total, ms_per_step):
+    """Whole-job kept TFLOP/s when the ranks split one workload: all of its
+    kept work in the slowest rank's step time."""
+    return kept_flop_total / (ms_per_step * 1e-3) / 1e12
+
+
+def step_stats(ms):
+    """Median, 10th and 90th percentile of per-step times (ms)."""
+    a = np.asarray(ms, dtype=np.float64)
+    return {"median": float(np.median(a)), "p10": float(np.percentile(a, 10)),
+            "p90": float(np.percentile(a, 90)), "mean": float(a.mean())}
 
 
 # ----------------------------------------------------------------- main legs
@@ -216,7 +249,8 @@ def run_reference(args, rank, world):
         return
     from workloads import make_workload
 
-    arrays, prm = make_workload(WORKLOAD)
+    name = getattr(args, "workload", WORKLOAD)
+    arrays, prm = make_workload(name)
     ncores = host_cores()
     pool = _oracle_pool(ncores)
     H = prm["H"]
@@ -243,11 +277,11 @@ def run_reference(args, rank, world):
         "warmup": args.warmup,
         "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": "strong",
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": workload_config(prm),
+        "config": workload_config(prm, name),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": ncores, "kind": "oracle",
                          "sample": f"{len(sample_heads)} of {H} heads per step, all rows"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -255,9 +289,21 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def workload_config(prm):
+WORKLOAD_TEXT = {
+    "tiny": "tiny: 1024 video + 128 context tokens, 2 heads, i.i.d. inputs",
+    "8k": "8192 video + 512 context tokens, 24 heads, block-clustered, zero key bias",
+    "h3": "H3-shaped packed video sequence (9240 video + 265 context tokens)",
+    "32k": "32768 video + 1024 context tokens, 40 heads, block-clustered, biased sinks",
+    "64k": "65560 video (pad tail) + 2048 context tokens, 24 heads, 3-D clustered, biased sinks",
+}
+
+
+def workload_config(prm, name=WORKLOAD):
+    qkvo = 4 * prm["T"] * prm["H"] * 128 * 2
+    l2 = ("inputs larger than L2 (Q+K+V+O %d MB > 126 MB), no flush" % (qkvo // 10**6) if qkvo > 126e6
+          else "inputs smaller than L2 (Q+K+V+O %d MB): L2 flushed before every step" % (qkvo // 10**6))
     return {
-        "workload": "H3-shaped packed video sequence (9240 video + 265 context tokens)",
+        "workload": WORKLOAD_TEXT[name],
         "T": prm["T"],
         "H": prm["H"],
         "head_dim": 128,
@@ -265,9 +311,17 @@ def workload_config(prm):
         "topk_ratio": prm["topk_ratio"],
         "radius": prm["radius"],
         "tail_mode": prm["tail_mode"],
-        "key_bias": None,
-        "l2": "inputs larger than L2 (Q+K+V+O 545 MB > 126 MB), no flush",
+        "key_bias": None if prm.get("bias_kind", "none") == "none" else prm["bias_kind"],
+        "l2": l2,
     }
+
+
+def _oracle_one_core(args):
+    """The oracle on a few heads in one process with one BLAS thread (runs in
+    a spawned process); returns (kept_flops, seconds)."""
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    return _oracle_worker(args)
 
 
 def run_ours(args, rank, world, local_rank):
@@ -277,22 +331,28 @@ def run_ours(args, rank, world, local_rank):
     import block_sparse_routed_gb300 as bsr
     from workloads import make_workload
 
-    # CPU baseline pool first: spawned before the first GPU call.
-    pool = None
+    # CPU baseline pools first: spawned before the first GPU call.
+    pool = pool1 = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         pool = _oracle_pool(host_cores())
+        pool1 = mp.get_context("spawn").Pool(1)
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     bsr.load_library()
-    arrays, prm = make_workload(WORKLOAD)
+    name = args.workload
+    arrays_all, prm = make_workload(name)
     T, H, Nv = prm["T"], prm["H"], prm["video_tokens"]
-    P = bsr.Params(T=T, H=H, video_tokens=Nv, topk_ratio=prm["topk_ratio"], radius=prm["radius"],
+    # this rank's heads (all of them on one GPU)
+    h0, h1 = head_range(H, rank, world)
+    arrays = split_heads(arrays_all, h0, h1)
+    Hr = h1 - h0
+    P = bsr.Params(T=T, H=Hr, video_tokens=Nv, topk_ratio=prm["topk_ratio"], radius=prm["radius"],
                    tail_mode=prm["tail_mode"])
     sz = bsr.sparse_attn_query(P)
 
     def pinned(bits):
-        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).reshape(1, T, H, 128).pin_memory()
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).reshape(1, T, Hr, 128).pin_memory()
 
     hq, hk, hv = pinned(arrays["q"]), pinned(arrays["k"]), pinned(arrays["v"])
     q, k, v = hq.to(dev), hk.to(dev), hv.to(dev)
@@ -300,12 +360,16 @@ def run_ours(args, rank, world, local_rank):
     if arrays["bias"] is not None:
         hbias = torch.from_numpy(arrays["bias"]).pin_memory()
         bias = hbias.to(dev)
-    idx = torch.empty((1, H, sz.nq, sz.maxl), dtype=torch.int32, device=dev)
-    cnt = torch.empty((1, H, sz.nq), dtype=torch.int32, device=dev)
+    idx = torch.empty((1, Hr, sz.nq, sz.maxl), dtype=torch.int32, device=dev)
+    cnt = torch.empty((1, Hr, sz.nq), dtype=torch.int32, device=dev)
     o = torch.empty_like(q)
     ws_plan = torch.empty(sz.plan_ws_bytes, dtype=torch.uint8, device=dev)
     ws_fwd = torch.empty(sz.fwd_ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    # small workloads fit in L2: flush it between steps (writes of a buffer
+    # larger than L2, outside the timed events)
+    qkvo = 4 * T * Hr * 128 * 2
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if qkvo <= 126e6 else None
 
     def step():
         bsr.sparse_attn_plan(P, q, k, idx=idx, cnt=cnt, ws=ws_plan, stream=stream)
@@ -316,8 +380,15 @@ def run_ours(args, rank, world, local_rank):
     st = bsr.sparse_attn_last_device_status(ws_fwd, stream)
     if st != 0:
         raise RuntimeError(f"device status {st} after warm-up")
-    kept = kept_pairs_from_lists(idx.cpu().numpy(), cnt.cpu().numpy(), T, sz.nvk, sz.nq, Nv,
-                                 sz.dense_row_start) * 4 * 128
+    kept_mine = kept_pairs_from_lists(idx.cpu().numpy(), cnt.cpu().numpy(), T, sz.nvk, sz.nq, Nv,
+                                      sz.dense_row_start) * 4 * 128
+    # the whole job's kept work (every rank's heads)
+    if world > 1:
+        t = torch.tensor([float(kept_mine)], dtype=torch.float64, device=dev)
+        dist.all_reduce(t)
+        kept = float(t.item())
+    else:
+        kept = float(kept_mine)
 
     def barrier():
         if world > 1:
@@ -333,31 +404,47 @@ def run_ours(args, rank, world, local_rank):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
-    for s in range(args.steps):
-        ev[s][0].record(stream)
+    for s_ in range(args.steps):
+        if flush is not None:
+            flush.fill_(s_ & 0xFF)
+        ev[s_][0].record(stream)
         bsr.sparse_attn_plan(P, q, k, idx=idx, cnt=cnt, ws=ws_plan, stream=stream)
-        ev[s][1].record(stream)
+        ev[s_][1].record(stream)
         bsr.sparse_attn_fwd(P, q, k, v, idx, cnt, key_bias=bias, o=o, ws=ws_fwd, stream=stream)
-        ev[s][2].record(stream)
+        ev[s_][2].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     barrier()
-    total_ms = t_start.elapsed_time(t_end)
-    plan_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
-    fwd_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(args.steps)]
+    plan_ms = [ev[s_][0].elapsed_time(ev[s_][1]) for s_ in range(args.steps)]
+    fwd_ms = [ev[s_][1].elapsed_time(ev[s_][2]) for s_ in range(args.steps)]
+    step_ms = [a_ + b_ for a_, b_ in zip(plan_ms, fwd_ms)]
+    total_ms = t_start.elapsed_time(t_end) if flush is None else sum(step_ms)
     if bsr.sparse_attn_last_device_status(ws_fwd, stream) != 0:
         raise RuntimeError("device status error in the timed region")
     total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
-    value = weak_scaling_value(kept, ms_per_step, world)
+    value = strong_scaling_value(kept, ms_per_step)
+
+    # ---- one cold-L2 leg: the forward with L2 flushed before every call
+    cold = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    cold_ms = []
+    for i in range(max(10, min(args.steps, 50))):
+        cold.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        bsr.sparse_attn_fwd(P, q, k, v, idx, cnt, key_bias=bias, o=o, ws=ws_fwd, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        cold_ms.append(e0.elapsed_time(e1))
+    del cold
 
     # ---- end to end through the public API, host buffers.  Every step copies
     # its inputs in from pinned host memory and its output back; steps are
     # pipelined over two buffer sets and three streams (copy in, compute,
     # copy out), so step i+1's inputs travel while step i computes.
-    h2d = 3 * T * H * 128 * 2 + (T * 4 if bias is not None else 0)
-    d2h = T * H * 128 * 2
+    h2d = 3 * T * Hr * 128 * 2 + (T * 4 if bias is not None else 0)
+    d2h = T * Hr * 128 * 2
     s_in, s_comp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     sets = []
     for _ in range(2):
@@ -366,29 +453,29 @@ def run_ours(args, rank, world, local_rank):
             bias=None if bias is None else torch.empty_like(bias), o=torch.empty_like(q),
             idx=torch.empty_like(idx), cnt=torch.empty_like(cnt),
             wp=torch.empty_like(ws_plan), wf=torch.empty_like(ws_fwd),
-            ho=torch.empty((1, T, H, 128), dtype=torch.bfloat16).pin_memory(),
+            ho=torch.empty((1, T, Hr, 128), dtype=torch.bfloat16).pin_memory(),
             ev_in=torch.cuda.Event(), ev_comp=torch.cuda.Event(), ev_out=torch.cuda.Event()))
 
     def e2e_step(i):
-        st = sets[i % 2]
+        st_ = sets[i % 2]
         with torch.cuda.stream(s_in):
-            s_in.wait_event(st["ev_comp"])  # step i-2 has read this set's inputs
-            st["q"].copy_(hq, non_blocking=True)
-            st["k"].copy_(hk, non_blocking=True)
-            st["v"].copy_(hv, non_blocking=True)
+            s_in.wait_event(st_["ev_comp"])  # step i-2 has read this set's inputs
+            st_["q"].copy_(hq, non_blocking=True)
+            st_["k"].copy_(hk, non_blocking=True)
+            st_["v"].copy_(hv, non_blocking=True)
             if bias is not None:
-                st["bias"].copy_(hbias, non_blocking=True)
-            st["ev_in"].record(s_in)
-        s_comp.wait_event(st["ev_in"])
-        s_comp.wait_event(st["ev_out"])  # step i-2's output has left this set
-        bsr.sparse_attn_plan(P, st["q"], st["k"], idx=st["idx"], cnt=st["cnt"], ws=st["wp"], stream=s_comp)
-        bsr.sparse_attn_fwd(P, st["q"], st["k"], st["v"], st["idx"], st["cnt"], key_bias=st["bias"],
-                            o=st["o"], ws=st["wf"], stream=s_comp)
-        st["ev_comp"].record(s_comp)
+                st_["bias"].copy_(hbias, non_blocking=True)
+            st_["ev_in"].record(s_in)
+        s_comp.wait_event(st_["ev_in"])
+        s_comp.wait_event(st_["ev_out"])  # step i-2's output has left this set
+        bsr.sparse_attn_plan(P, st_["q"], st_["k"], idx=st_["idx"], cnt=st_["cnt"], ws=st_["wp"], stream=s_comp)
+        bsr.sparse_attn_fwd(P, st_["q"], st_["k"], st_["v"], st_["idx"], st_["cnt"], key_bias=st_["bias"],
+                            o=st_["o"], ws=st_["wf"], stream=s_comp)
+        st_["ev_comp"].record(s_comp)
         with torch.cuda.stream(s_out):
-            s_out.wait_event(st["ev_comp"])
-            st["ho"].copy_(st["o"], non_blocking=True)
-            st["ev_out"].record(s_out)
+            s_out.wait_event(st_["ev_comp"])
+            st_["ho"].copy_(st_["o"], non_blocking=True)
+            st_["ev_out"].record(s_out)
 
     for i in range(2):
         e2e_step(i)
@@ -399,40 +486,54 @@ def run_ours(args, rank, world, local_rank):
     e0.record(s_in)
     for i in range(args.steps):
         e2e_step(i)
-    for st in sets:
-        s_out.wait_event(st["ev_out"])
+    for st_ in sets:
+        s_out.wait_event(st_["ev_out"])
     e1.record(s_out)
     torch.cuda.synchronize(dev)
-    for st in sets:
-        if bsr.sparse_attn_last_device_status(st["wf"], s_comp) != 0:
+    for st_ in sets:
+        if bsr.sparse_attn_last_device_status(st_["wf"], s_comp) != 0:
             raise RuntimeError("device status error in the end-to-end run")
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
-    e2e_value = weak_scaling_value(kept, e2e_ms, world)
+    e2e_value = strong_scaling_value(kept, e2e_ms)
+    # the whole job's copies (every rank's heads)
+    h2d_all = 3 * T * H * 128 * 2 + (T * 4 * world if bias is not None else 0)
+    d2h_all = T * H * 128 * 2
 
     if rank != 0:
         return
 
     peaks, peak_kind = measured_peaks()
     fwd_avg = sum(fwd_ms) / len(fwd_ms)
-    achieved = kept / (fwd_avg * 1e-3) / 1e12
+    achieved = kept_mine / (fwd_avg * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": profile_traffic(),
+                "frac": achieved / peak, "traffic": profile_traffic() if name == WORKLOAD and world == 1 else None,
                 "kernel": "attention_kernel (fwd call: status memset + attention)",
                 "peak_kind": f"{peak_kind} bf16 burst"}
 
-    cpu = None
+    cpu = cpu1 = None
     if pool is not None:
         try:
             heads = list(range(H))
-            flops_c, secs_c = oracle_timing(pool, arrays, prm, 1, host_cores(), heads)
+            flops_c, secs_c = oracle_timing(pool, arrays_all, prm, 1, host_cores(), heads)
             cpu = {"value": flops_c / secs_c / 1e12, "unit": "TFLOP/s", "cores": host_cores(),
                    "kind": "oracle", "seconds": secs_c,
                    "sample": f"whole workload ({H} heads, all rows), one head per task, "
                              f"one BLAS thread per worker"}
+            # one core: a bounded sample of whole heads, one process, one BLAS thread
+            nh1 = 1 if T > 20000 else 2
+            hs = list(range(nh1))
+            f1, s1 = pool1.apply(_oracle_one_core, ((np.ascontiguousarray(arrays_all["q"][:, hs]),
+                                                      np.ascontiguousarray(arrays_all["k"][:, hs]),
+                                                      np.ascontiguousarray(arrays_all["v"][:, hs]),
+                                                      arrays_all["bias"], prm),))
+            cpu1 = {"value": f1 / s1 / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "seconds": s1,
+                    "sample": f"{nh1} of {H} heads, all rows, one process, one BLAS thread"}
         finally:
             pool.close()
             pool.join()
+            pool1.close()
+            pool1.join()
 
     line = {
         "metric": METRIC,
@@ -443,19 +544,25 @@ def run_ours(args, rank, world, local_rank):
         "warmup": args.warmup,
         "ms_per_step": ms_per_step,
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": "strong",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": workload_config(prm),
+        "config": dict(workload_config(prm, name),
+                       **({"parallelism": f"heads split over {world} ranks"} if world > 1 else {})),
         "plan_ms": sum(plan_ms) / len(plan_ms),
         "fwd_ms": fwd_avg,
+        "step_ms_stats": step_stats(step_ms),
+        "fwd_ms_stats": step_stats(fwd_ms),
+        "plan_ms_stats": step_stats(plan_ms),
+        "fwd_ms_cold_l2": step_stats(cold_ms),
         "kept_tflop_per_step": kept / 1e12,
         "frac_of_bf16_peak": value / world / peak,
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+        "cpu_baseline_1core": cpu1,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d_all,
+                "d2h_bytes_per_step": d2h_all, "ms_per_step": e2e_ms,
                 "pipeline": "2 buffer sets, copy-in / compute / copy-out streams"},
         "gpu_launches": args.steps * (3 + (1 if bias is not None else 0)),
         "clocks": clk,
@@ -828,11 +935,12 @@ def run_spark(args, rank, world, local_rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--op", choices=["attention", "reweight", "spark", "reblock"], default="attention")
+    ap.add_argument("--workload", choices=["tiny", "8k", "h3", "32k", "64k"], default=WORKLOAD)
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

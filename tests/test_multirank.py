@@ -1,12 +1,13 @@
 """The N > 1 path on CPU: two `gloo` ranks, no GPU.
 
-bench.py under torchrun runs one independent copy of the workload per rank
-(heads and problems are independent; no collective in the data path) and
-reports the whole job's throughput over the slowest rank's time.  These tests
-run its rank helpers in two spawned processes, check that a reference run on
-a nonzero rank does no work, and check the property the sharding rests on:
-the plan and the output of every head depend on that head's inputs only, so
-heads split across ranks and gathered give the single-process result.
+bench.py under torchrun splits the heads into contiguous slices, one per rank
+(heads are independent; no collective in the data path), and reports the
+whole job's kept work over the slowest rank's time (strong scaling).  These
+tests run its rank helpers (bench.head_range, bench.split_heads) in two
+spawned processes, check that a reference run on a nonzero rank does no work,
+and check the property the sharding rests on: the plan and the output of
+every head depend on that head's inputs only, so the ranks' slices, gathered,
+give the single-process result.
 """
 
 import os
@@ -42,16 +43,17 @@ def _rank_main(rank, world, port, q):
         # slowest rank's time; identity on one rank
         out["max"] = bench.max_over_ranks(1.5 + rank, world, "cpu")
         out["single"] = bench.max_over_ranks(1.5 + rank, 1, "cpu")
-        out["value"] = bench.weak_scaling_value(2.0e12, 4.0, world)
+        out["value"] = bench.strong_scaling_value(2.0e12, 4.0)
 
         # heads rank::world of the tiny workload, gathered on every rank
         arrays, prm = make_workload("tiny")
         sz = O.derive_sizes(prm["T"], prm["H"], prm["video_tokens"], prm["topk_ratio"],
                             prm["radius"], prm["tail_mode"])
-        mine = list(range(rank, prm["H"], world))
-        qh = np.ascontiguousarray(arrays["q"][:, mine])
-        kh = np.ascontiguousarray(arrays["k"][:, mine])
-        vh = np.ascontiguousarray(arrays["v"][:, mine])
+        h0, h1 = bench.head_range(prm["H"], rank, world)
+        mine = list(range(h0, h1))
+        sl = bench.split_heads(arrays, h0, h1)
+        qh, kh, vh = sl["q"], sl["k"], sl["v"]
+        assert qh.flags["C_CONTIGUOUS"] and qh.shape[1] == len(mine)
         szh = O.derive_sizes(prm["T"], len(mine), prm["video_tokens"], prm["topk_ratio"],
                              prm["radius"], prm["tail_mode"])
         ref = O.plan(qh, kh, szh)
@@ -98,9 +100,21 @@ def test_time_is_the_slowest_rank(two_ranks):
         assert two_ranks[r]["single"] == 1.5 + r
 
 
-def test_weak_scaling_value_counts_every_rank(two_ranks):
-    # two copies of 2 TFLOP in 4 ms
-    assert two_ranks[0]["value"] == pytest.approx(2 * 2.0e12 / 4.0e-3 / 1e12)
+def test_strong_scaling_value_is_the_job_work_over_the_slowest_rank(two_ranks):
+    # one workload of 2 TFLOP split over the ranks, 4 ms for the slowest
+    assert two_ranks[0]["value"] == pytest.approx(2.0e12 / 4.0e-3 / 1e12)
+
+
+def test_head_ranges_partition_the_heads():
+    import bench
+
+    for H in (1, 2, 5, 24, 56):
+        for world in (1, 2, 3, 4, 8):
+            rs = [bench.head_range(H, r, world) for r in range(world)]
+            assert rs[0][0] == 0 and rs[-1][1] == H
+            assert all(rs[i][1] == rs[i + 1][0] for i in range(world - 1))
+            sizes = [b - a for a, b in rs]
+            assert max(sizes) - min(sizes) <= 1
 
 
 def test_heads_split_across_ranks_give_the_single_process_result(two_ranks):

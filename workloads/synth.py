@@ -182,6 +182,7 @@ def make_workload(name: str):
         topk_ratio=w.topk_ratio,
         radius=w.radius,
         tail_mode=w.tail_mode,
+        bias_kind=w.bias_kind,
     )
     return arrays, params
 
