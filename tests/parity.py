@@ -98,6 +98,25 @@ def _oracle_head(args):
     return O.forward_merged(qh, kh, vh, bias, idx_h, cnt_h, sz, s["ak16"][0], s["av16"][0], s["lm"][0])[:, 0]
 
 
+def _reblock_margin_head(args):
+    """The margin-rule check of one head's permutation against the float64
+    reblocking tree (runs in a spawned worker): (violations, coverage)."""
+    bits_h, perm_h, fanout, L, depth = args
+    from oracle import reblock_f64 as F
+
+    p64, nodes = F.reblock_tree(bits_h, fanout, L, depth)
+    return F.check_permutation(perm_h, p64, nodes, bits_h.shape[0])
+
+
+def reblock_margin_all(pool, x_bits, perm, fanout, L, depth, heads=None):
+    """Margin-rule checks of perm [H, T] against the float64 tree of every
+    (or the listed) head of x_bits [T, H, 128]: a list of (head, violations,
+    coverage)."""
+    heads = list(range(x_bits.shape[1])) if heads is None else list(heads)
+    tasks = [(np.ascontiguousarray(x_bits[:, h, :]), np.asarray(perm[h]), fanout, L, depth) for h in heads]
+    return [(h, v, c) for h, (v, c) in zip(heads, pool.map(_reblock_margin_head, tasks, chunksize=1))]
+
+
 def oracle_pool(max_workers=16):
     """A spawned process pool for the oracle (safe after CUDA is initialised),
     one BLAS thread per worker."""

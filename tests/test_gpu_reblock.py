@@ -1,5 +1,9 @@
-"""Parity of the CUDA reblocking (sparse_attn_spark_reblock) with the oracle
-(oracle/reblock.py): the permutation and its inverse must match bit for bit.
+"""Parity of the CUDA reblocking (sparse_attn_spark_reblock) with the oracles:
+bit for bit against the fixed-order FP32 statement (oracle/reblock.py, the
+numeric contract), and under the margin rule against the float64 tree
+(oracle/reblock_f64.py: ordinary dot products, no fixed order), which must
+agree with the kernel on every decision whose margin exceeds the float32
+error bound.
 
 Source: "Sol-Attn and Spark for MiniMax-H3", section "Spark primitives"
 (spark_reblock) and section "Spark inference integration" (power-of-two
@@ -15,6 +19,7 @@ import numpy as np
 import pytest
 
 from oracle import reblock as R
+from tests.parity import oracle_pool, reblock_margin_all
 from workloads import make_workload
 
 pytestmark = pytest.mark.gpu
@@ -158,3 +163,50 @@ def test_argument_errors(bsr):
             bsr.spark_reblock(x, **kw)
     with pytest.raises(ValueError):
         bsr.spark_reblock(x.float(), fanout=8)
+
+
+# ---------------------------------------------------------------- float64 tree, margin rule
+@pytest.fixture(scope="module")
+def pool():
+    p = oracle_pool()
+    yield p
+    p.close()
+    p.join()
+
+
+def _margin(bsr, pool, name, xb, fanout, heads=None, L=32):
+    """The kernel's permutation against the float64 tree, for any summation
+    order (depth 127) and for the contract's depth 8; logs the coverage."""
+    perm, _ = bsr.spark_reblock(_dev(xb), fanout=fanout, landmarks=L)
+    perm = perm.cpu().numpy()
+    for depth in (127, 8):
+        res = reblock_margin_all(pool, xb, perm, fanout, L, depth, heads)
+        bad = [(h, v[:2]) for h, v, _ in res if v]
+        cov = [c for _, _, c in res]
+        print(f"[reblock margin] {name} fanout {fanout} depth {depth}: {len(res)} heads, "
+              f"leaf-certain tokens {np.mean(cov):.3f} (min {np.min(cov):.3f})")
+        assert not bad, bad
+    return perm
+
+
+@pytest.mark.parametrize("T,H,fanout", [(64 * 7 + 13, 3, 2), (64 * 20 + 1, 2, 8), (64 * 33 + 63, 2, 16),
+                                        (64 * 11 + 3, 2, 4)])
+def test_margin_rule_random_samples(bsr, pool, T, H, fanout):
+    rng = np.random.default_rng(T * 7 + fanout)
+    _margin(bsr, pool, f"T={T}", _bits(rng.standard_normal((T, H, 128))), fanout)
+
+
+def test_margin_rule_h3_keys_all_heads(bsr, pool):
+    arrays, _ = make_workload("h3")
+    _margin(bsr, pool, "h3 keys", arrays["k"], 8)
+
+
+def test_margin_rule_h3_queries_fanout16(bsr, pool):
+    arrays, _ = make_workload("h3")
+    _margin(bsr, pool, "h3 queries", arrays["q"], 16, heads=range(0, 56, 4))
+
+
+@pytest.mark.parametrize("name,heads", [("8k", [0, 7, 23]), ("32k", [0, 13, 39]), ("64k", [0, 23])])
+def test_margin_rule_other_configs(bsr, pool, name, heads):
+    arrays, _ = make_workload(name)
+    _margin(bsr, pool, f"{name} keys", arrays["k"], 8, heads=heads)

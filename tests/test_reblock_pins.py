@@ -1,5 +1,6 @@
-"""Pins of the reblocking oracle (oracle/reblock.py) to facts that do not come
-from the oracle itself: hand-worked splits of orthogonal token groups (child
+"""Pins of the reblocking oracles (the fixed-order FP32 statement in
+oracle/reblock.py and the float64 tree in oracle/reblock_f64.py) to facts
+that do not come from either oracle: hand-worked splits of orthogonal token groups (child
 order, the farthest-pair tie rule, stable parent order), the closed form of
 tokens on a planar arc (every split is by angle, so the blocks are the runs
 of 64 of the angle order), landmark positions (decoy tokens off the landmark
@@ -17,6 +18,16 @@ import numpy as np
 import pytest
 
 from oracle import reblock as R
+from oracle import reblock_f64 as F
+
+IMPLS = ["fp32", "fp64"]
+
+
+def _perm(impl, bits, fanout):
+    """The permutation of one head by the FP32 statement or the float64 tree."""
+    if impl == "fp32":
+        return R.reblock_head(bits, fanout)[0]
+    return F.reblock_tree(bits, fanout)[0]
 
 
 def _bits(x):
@@ -40,17 +51,18 @@ def _groups(ng, T):
     return _bits(x)
 
 
-def test_child_counts_are_powers_of_two_up_to_the_fanout():
-    assert R.child_blocks(148, 8) == [19, 19, 19, 19, 18, 18, 18, 18]
-    assert R.child_blocks(19, 8) == [3, 3, 3, 2, 2, 2, 2, 2]
-    assert R.child_blocks(3, 8) == [2, 1]
-    assert R.child_blocks(5, 4) == [2, 1, 1, 1]
-    assert R.child_blocks(7, 16) == [2, 2, 2, 1]
-    assert R.child_blocks(20, 16) == [2, 2, 2, 2] + [1] * 12
-    assert R.child_blocks(2, 2) == [1, 1]
+@pytest.mark.parametrize("child_blocks", [R.child_blocks, F.children_sizes], ids=IMPLS)
+def test_child_counts_are_powers_of_two_up_to_the_fanout(child_blocks):
+    assert child_blocks(148, 8) == [19, 19, 19, 19, 18, 18, 18, 18]
+    assert child_blocks(19, 8) == [3, 3, 3, 2, 2, 2, 2, 2]
+    assert child_blocks(3, 8) == [2, 1]
+    assert child_blocks(5, 4) == [2, 1, 1, 1]
+    assert child_blocks(7, 16) == [2, 2, 2, 1]
+    assert child_blocks(20, 16) == [2, 2, 2, 2] + [1] * 12
+    assert child_blocks(2, 2) == [1, 1]
     for m in range(2, 300):
         for f in (2, 4, 8, 16):
-            s = R.child_blocks(m, f)
+            s = child_blocks(m, f)
             c = len(s)
             assert c & (c - 1) == 0 and c <= min(f, m) < 2 * c
             assert sum(s) == m and max(s) - min(s) <= 1 and s == sorted(s, reverse=True)
@@ -63,7 +75,8 @@ def test_landmarks_sit_on_the_even_grid():
     assert R.landmark_positions(10, 32) == list(range(10))
 
 
-def test_two_orthogonal_groups_hand_worked():
+@pytest.mark.parametrize("impl", IMPLS)
+def test_two_orthogonal_groups_hand_worked(impl):
     # Tokens 0-63 along e0, 64-127 along e1, 5 remainder tokens.  Landmarks
     # are positions 0, 4, ..., 124; every cross pair has cosine 0 (the
     # minimum), the first one is landmarks (0, 16): a = token 0 (e0),
@@ -72,23 +85,23 @@ def test_two_orthogonal_groups_hand_worked():
     T = 133
     x = _groups(2, T)
     for fanout in (2, 8):
-        perm, inv = R.reblock_head(x, fanout)
+        perm = _perm(impl, x, fanout)
         assert perm.tolist() == list(range(64, 128)) + list(range(64)) + list(range(128, 133))
-        assert np.array_equal(inv[perm], np.arange(T))
 
 
-def test_four_orthogonal_groups_hand_worked():
+@pytest.mark.parametrize("impl", IMPLS)
+def test_four_orthogonal_groups_hand_worked(impl):
     # Landmarks every 8 tokens: 0-7 in group 0, 8-15 group 1, ...  The first
     # pair with cosine 0 is (0, 8): a = group 0, b = group 1.  kappa: group 1
     # -1, groups 2 and 3 0 (ranked by position), group 0 +1.
     x = _groups(4, 256)
-    perm, _ = R.reblock_head(x, 4)
+    perm = _perm(impl, x, 4)
     assert perm.tolist() == list(range(64, 128)) + list(range(128, 256)) + list(range(64))
     # with fanout 2 the root splits 2 + 2 blocks: child 0 = groups 1 and 2,
     # child 1 = groups 3 and 0 in parent order (0 then 3).  Child 0 (256
     # -> 128 tokens, landmarks every 4): pair (0, 16) = (group 1, group 2),
     # so group 2 comes first; child 1: pair (group 0, group 3), group 3 first.
-    perm, _ = R.reblock_head(x, 2)
+    perm = _perm(impl, x, 2)
     assert perm.tolist() == (list(range(128, 192)) + list(range(64, 128))
                              + list(range(192, 256)) + list(range(64)))
 
@@ -114,8 +127,9 @@ def _arc_tokens(rng, n, lo_deg, hi_deg, rem=0):
     return bits, theta
 
 
+@pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("fanout", [2, 4, 8, 16])
-def test_planar_arc_blocks_are_runs_of_the_angle_order(fanout):
+def test_planar_arc_blocks_are_runs_of_the_angle_order(fanout, impl):
     # On an arc shorter than 180 degrees the farthest landmarks are the
     # arc's extremes among the landmarks and kappa is monotone in the angle,
     # in every node: each block is 64 tokens consecutive in angle, and inside
@@ -123,7 +137,7 @@ def test_planar_arc_blocks_are_runs_of_the_angle_order(fanout):
     rng = np.random.default_rng(100 + fanout)
     n = 512
     bits, theta = _arc_tokens(rng, n, 5.0, 175.0, rem=7)
-    perm, inv = R.reblock_head(bits, fanout)
+    perm = _perm(impl, bits, fanout)
     want = {tuple(sorted(np.argsort(theta[:n])[64 * b:64 * (b + 1)].tolist())) for b in range(n // 64)}
     got = [perm[64 * b:64 * (b + 1)].tolist() for b in range(n // 64)]
     assert {tuple(g) for g in got} == want
@@ -132,7 +146,8 @@ def test_planar_arc_blocks_are_runs_of_the_angle_order(fanout):
     assert perm[n:].tolist() == list(range(n, n + 7))
 
 
-def test_decoys_off_the_landmark_grid_do_not_span_the_split():
+@pytest.mark.parametrize("impl", IMPLS)
+def test_decoys_off_the_landmark_grid_do_not_span_the_split(impl):
     # 256 tokens, fanout 4: one split of the root into 4 leaves.  254 tokens
     # sit on an evenly spaced grid from 0 to 90 degrees with the two ends at
     # landmark positions 0 and 248 (landmarks are every 8th position), so
@@ -156,7 +171,7 @@ def test_decoys_off_the_landmark_grid_do_not_span_the_split():
     theta = np.arctan2(xd @ u2, xd @ u1)
     kappa = np.cos(theta - theta[0]) - np.cos(theta - theta[248])
     order = np.lexsort((np.arange(n), kappa))
-    perm, _ = R.reblock_head(bits, 4)
+    perm = _perm(impl, bits, 4)
     for b in range(4):
         assert perm[64 * b:64 * (b + 1)].tolist() == sorted(order[64 * b:64 * (b + 1)].tolist())
     assert 25 in perm[:64] and 167 in perm[192:256]
@@ -179,7 +194,8 @@ def test_permutation_invariants(T, fanout):
     assert out["blocks"].shape == (2, N // 64, 64) and out["excluded"].shape == (2, T - N)
 
 
-def test_scale_and_degenerate_rows():
+@pytest.mark.parametrize("impl", IMPLS)
+def test_scale_and_degenerate_rows(impl):
     # a positive scale per token changes nothing (cosine distance); identical
     # rows make every kappa 0, so every split keeps the flat order
     rng = np.random.default_rng(3)
@@ -187,14 +203,14 @@ def test_scale_and_degenerate_rows():
     x = rng.standard_normal((T, 128)).astype(np.float32)
     # powers of two keep the BF16 rounding of every row's direction exact
     s = (2.0 ** rng.integers(-6, 7, T)).astype(np.float32)
-    p0, _ = R.reblock_head(_bits(x), 8)
-    p1, _ = R.reblock_head(_bits(x * s[:, None]), 8)
+    p0 = _perm(impl, _bits(x), 8)
+    p1 = _perm(impl, _bits(x * s[:, None]), 8)
     assert np.array_equal(p0, p1)
     same = np.tile(_bits(rng.standard_normal(128))[None], (T, 1))
-    p2, _ = R.reblock_head(same, 8)
+    p2 = _perm(impl, same, 8)
     assert p2.tolist() == list(range(T))
     zero = np.zeros((T, 128), dtype=np.uint16)
-    p3, _ = R.reblock_head(zero, 4)
+    p3 = _perm(impl, zero, 4)
     assert p3.tolist() == list(range(T))
 
 
