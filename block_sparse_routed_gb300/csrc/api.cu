@@ -246,6 +246,7 @@ SA_API sa_status sparse_attn_fwd(const sa_params* p, const void* q, const void* 
   a.o = static_cast<uint16_t*>(o);
   a.status = status;
   a.unit_counter = status + 1;  // inside the status area, cleared above
+  a.bias_nz = status + 2;
   a.g = g;
   a.n_dense = (g.T - g.r0 + 127) / 128;
   a.n_pairs = (g.nq + 1) / 2;
@@ -335,6 +336,7 @@ SA_API sa_status sparse_attn_fused(const sa_params* p, const void* q, const void
   a.o = static_cast<uint16_t*>(o);
   a.status = status;
   a.unit_counter = status + 1;  // inside the status area, cleared above
+  a.bias_nz = status + 2;
   a.g = g;
   a.n_dense = (g.T - g.r0 + 127) / 128;
   a.n_pairs = (g.nq + 1) / 2;
@@ -425,6 +427,7 @@ SA_API sa_status sparse_attn_spark_fwd(const sa_params* p, const void* q, const 
   a.o = static_cast<uint16_t*>(o);
   a.status = status;
   a.unit_counter = status + 1;  // inside the status area, cleared above
+  a.bias_nz = status + 2;
   a.g = g;
   a.n_dense = (g.T - g.r0 + 127) / 128;
   a.n_pairs = (g.nq + 1) / 2;

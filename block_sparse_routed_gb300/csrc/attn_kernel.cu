@@ -769,6 +769,9 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     const int half = row >> 6;
     const float sl2 = a.scale_log2;
+    // An all-zero key bias takes the no-bias path, so that it gives the same
+    // output bit for bit (the bias prep flags any nonzero value).
+    const bool key_bias = a.b2 != nullptr && *a.bias_nz != 0;
     float* rref = xchg;                    // [3][128]: reference after step g at g % 3
     float* xl = xchg + 3 * 128;            // [2][128]: partial row sums
     int G = 0;
@@ -824,7 +827,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int hh = 0; hh < 2; ++hh) {
           row_ok[hh] = (bits[hh] >> half) & 1;  // uniform across the warp
           nvalid[hh] = virt[hh] ? kBlock : min(kBlock, g.T - blk[hh] * kBlock);
-          add_bias[hh] = virt[hh] || ((a.b2 != nullptr) && blk[hh] >= g.nvk);
+          add_bias[hh] = virt[hh] || (key_bias && blk[hh] >= g.nvk);
           fast[hh] = row_ok[hh] && nvalid[hh] == kBlock && !add_bias[hh];
           if (!row_ok[hh]) continue;
           uint32_t sh[64];
@@ -832,11 +835,15 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           tmem_ld32(scol + 64u * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&sh[32]));
           tmem_wait_ld();
           // Logit in log2 units: l = s * log2(e)/sqrt(128) + b2 (b2 = 0 off
-          // sinks).  Both paths round identically where b2 = 0: the maximum
-          // of fma(s, c, 0) equals c * max(s), and p = 2^fma(s, c, b2 - ref).
+          // sinks).  A full half without additive logits needs only its
+          // maximum here (c * max(s) is the maximum of the rounded c * s);
+          // pass 2 forms p = 2^fma(s, c, -ref) from the scores.
           if (fast[hh]) {
             mx = fmaxf(mx, max64(sh) * sl2);
           } else {
+            // General half: the logits l = s * scale + b (-inf past the
+            // sequence end) replace the scores in tensor memory, so the
+            // bias is read once and pass 2 runs the packed path on them.
             const float4* bb = bias_of(hh);
 #pragma unroll
             for (int q4 = 0; q4 < 16; ++q4) {
@@ -845,14 +852,16 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int kx = 4 * q4 + e;
-                const bool valid = kx < nvalid[hh];
-                const float bk = valid ? bq[e] : 0.f;
-                const float x = fmaf(__uint_as_float(sh[kx]), sl2, bk);
-                if (valid) mx = fmaxf(mx, x);
+                const float x = (kx < nvalid[hh]) ? fmaf(__uint_as_float(sh[kx]), sl2, bq[e]) : -INFINITY;
+                sh[kx] = __float_as_uint(x);
+                mx = fmaxf(mx, x);
               }
             }
+            tmem_st32(scol + 64u * hh, *reinterpret_cast<uint32_t(*)[32]>(&sh[0]));
+            tmem_st32(scol + 64u * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&sh[32]));
           }
         }
+        if (!fast[0] || !fast[1]) tmem_wait_st();  // pass 2 reads the logits back
         // reference after step g-1 of this unit (published by the other group)
         if (j > 0) {
           if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(BAR_MREADY + (gs - 1) % 3), ((gs - 1) / 3) & 1,
@@ -889,9 +898,12 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tmem_ld32(scol + 64u * hh, *reinterpret_cast<uint32_t(*)[32]>(&sh[0]));
             tmem_ld32(scol + 64u * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&sh[32]));
             tmem_wait_ld();
-            if (fast[hh]) {
-              // p = 2^(s * scale - ref): one packed FMA per pair, one MUFU per value
-              const uint64_t sc2 = f2(sl2, sl2);
+            {
+              // p = 2^(x * c - ref): one packed FMA per pair, one MUFU per
+              // value; x is a score (c = scale) or, on a general half, a
+              // logit from pass 1 (c = 1).
+              const float c = fast[hh] ? sl2 : 1.0f;
+              const uint64_t sc2 = f2(c, c);
               const uint64_t nm2 = f2(-msub, -msub);
 #pragma unroll
               for (int kx = 0; kx < 64; kx += 2) {
@@ -900,26 +912,6 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
                 acc[(kx >> 1) & 3] = fadd2(acc[(kx >> 1) & 3], f2(e0, e1));
                 p[kx / 2] = pack_bf16x2(e0, e1);
-              }
-            } else {
-              const float4* bb = bias_of(hh);
-#pragma unroll
-              for (int q4 = 0; q4 < 16; ++q4) {
-                const float4 bv = add_bias[hh] ? bias_ld(bb + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
-                const float bq[4] = {bv.x, bv.y, bv.z, bv.w};
-                float e[4];
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                  const int kx = 4 * q4 + t;
-                  const bool valid = kx < nvalid[hh];
-                  const float bk = valid ? bq[t] : 0.f;
-                  const float x = fmaf(__uint_as_float(sh[kx]), sl2, bk - msub);
-                  e[t] = valid ? ex2_approx(x) : 0.f;
-                }
-                acc[(2 * q4) & 3] = fadd2(acc[(2 * q4) & 3], f2(e[0], e[1]));
-                acc[(2 * q4 + 1) & 3] = fadd2(acc[(2 * q4 + 1) & 3], f2(e[2], e[3]));
-                p[2 * q4] = pack_bf16x2(e[0], e[1]);
-                p[2 * q4 + 1] = pack_bf16x2(e[2], e[3]);
               }
             }
           }
@@ -1035,7 +1027,8 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Key bias: log2 conversion and the sink-only rule.
+// Key bias: log2 conversion, the sink-only rule, and the flag (status word
+// 2) that some bias value is nonzero.
 __global__ void bias_prep_kernel(const float* __restrict__ bias, float* __restrict__ b2,
                                  int32_t* status, int T, int video_keys) {
   const float kLog2e = 1.4426950408889634f;
@@ -1046,6 +1039,7 @@ __global__ void bias_prep_kernel(const float* __restrict__ bias, float* __restri
     } else if (u < video_keys && b != 0.0f) {
       set_status(status, 3 /* SA_ENOSINKBIAS */);
     }
+    if (b != 0.0f) status[2] = 1;  // some bias is nonzero (-0 counts as zero)
     b2[u] = b * kLog2e;
   }
 }

@@ -47,6 +47,7 @@ struct AttnArgs {
   uint16_t* o;         // BF16 bits [T, H, 128]
   int32_t* status;     // device status word
   int32_t* unit_counter;  // next work unit (zeroed before the launch)
+  const int32_t* bias_nz; // 1 when some key bias is nonzero (set by the bias prep)
   Geometry g;
   int n_dense;         // dense 128-row tiles per head
   int n_pairs;         // sparse query-block pairs per head
