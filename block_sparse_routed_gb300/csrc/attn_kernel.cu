@@ -823,13 +823,39 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // ordinary (coherent) loads, ordered after the descriptor barrier.
         auto bias_ld = [&](const float4* p) { return kMerged ? *p : __ldg(p); };
         float mx = -INFINITY;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+        auto half_flags = [&](int hh) {
           row_ok[hh] = (bits[hh] >> half) & 1;  // uniform across the warp
           nvalid[hh] = virt[hh] ? kBlock : min(kBlock, g.T - blk[hh] * kBlock);
           add_bias[hh] = virt[hh] || (key_bias && blk[hh] >= g.nvk);
           fast[hh] = row_ok[hh] && nvalid[hh] == kBlock && !add_bias[hh];
-          if (!row_ok[hh]) continue;
+        };
+        if constexpr (kMerged) {
+          half_flags(0);
+          half_flags(1);
+        }
+        // Both passes walk the two halves taking each half's flags by scalar
+        // selects, so that the loops can stay rolled without local memory:
+        // the merged build rolls them (one copy of the code; the
+        // tensor-memory loads order the halves anyway), measured faster
+        // there and slower in the exact build.
+        uint32_t ok_m = 0, fast_m = 0, bias_m = 0;
+        const float4* bb0 = nullptr;
+        const float4* bb1 = nullptr;
+        if constexpr (kMerged) {
+          ok_m = (row_ok[0] ? 1u : 0u) | (row_ok[1] ? 2u : 0u);
+          fast_m = (fast[0] ? 1u : 0u) | (fast[1] ? 2u : 0u);
+          bias_m = (add_bias[0] ? 1u : 0u) | (add_bias[1] ? 2u : 0u);
+          bb0 = bias_of(0);
+          bb1 = bias_of(1);
+        }
+        auto flag = [&](uint32_t m, const bool (&f)[2], int hh) -> bool {
+          if constexpr (kMerged) return (m >> hh) & 1u;
+          return f[hh];
+        };
+#pragma unroll(kMerged ? 1 : 2)
+        for (int hh = 0; hh < 2; ++hh) {
+          if constexpr (!kMerged) half_flags(hh);  // unrolled: constant index
+          if (!flag(ok_m, row_ok, hh)) continue;
           uint32_t sh[64];
           tmem_ld32(scol + 64u * hh, *reinterpret_cast<uint32_t(*)[32]>(&sh[0]));
           tmem_ld32(scol + 64u * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&sh[32]));
@@ -838,21 +864,23 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           // sinks).  A full half without additive logits needs only its
           // maximum here (c * max(s) is the maximum of the rounded c * s);
           // pass 2 forms p = 2^fma(s, c, -ref) from the scores.
-          if (fast[hh]) {
+          if (flag(fast_m, fast, hh)) {
             mx = fmaxf(mx, max64(sh) * sl2);
           } else {
             // General half: the logits l = s * scale + b (-inf past the
             // sequence end) replace the scores in tensor memory, so the
             // bias is read once and pass 2 runs the packed path on them.
-            const float4* bb = bias_of(hh);
+            const float4* bb = kMerged ? (hh ? bb1 : bb0) : bias_of(hh);
+            const bool ab = flag(bias_m, add_bias, hh);
+            const int nv = kMerged ? (hh ? nvalid[1] : nvalid[0]) : nvalid[hh];
 #pragma unroll
             for (int q4 = 0; q4 < 16; ++q4) {
-              const float4 bv = add_bias[hh] ? bias_ld(bb + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
+              const float4 bv = ab ? bias_ld(bb + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
               const float bq[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int kx = 4 * q4 + e;
-                const float x = (kx < nvalid[hh]) ? fmaf(__uint_as_float(sh[kx]), sl2, bq[e]) : -INFINITY;
+                const float x = (kx < nv) ? fmaf(__uint_as_float(sh[kx]), sl2, bq[e]) : -INFINITY;
                 sh[kx] = __float_as_uint(x);
                 mx = fmaxf(mx, x);
               }
@@ -887,10 +915,10 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         uint64_t acc[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[q] = f2(0.f, 0.f);
-#pragma unroll
+#pragma unroll(kMerged ? 1 : 2)
         for (int hh = 0; hh < 2; ++hh) {
           uint32_t p[32];
-          if (!row_ok[hh]) {
+          if (!flag(ok_m, row_ok, hh)) {
 #pragma unroll
             for (int kx = 0; kx < 32; ++kx) p[kx] = 0u;
           } else {
@@ -902,7 +930,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
               // p = 2^(x * c - ref): one packed FMA per pair, one MUFU per
               // value; x is a score (c = scale) or, on a general half, a
               // logit from pass 1 (c = 1).
-              const float c = fast[hh] ? sl2 : 1.0f;
+              const float c = flag(fast_m, fast, hh) ? sl2 : 1.0f;
               const uint64_t sc2 = f2(c, c);
               const uint64_t nm2 = f2(-msub, -msub);
 #pragma unroll
