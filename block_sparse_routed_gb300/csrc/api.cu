@@ -221,7 +221,7 @@ SA_API sa_status sparse_attn_fwd(const sa_params* p, const void* q, const void* 
   sa_status st = derive(p, &g, &sz);
   if (st != SA_OK) return st;
   if (!q || !k || !v || !idx || !cnt || !o || !ws) return SA_EINVAL;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 32) ||
       !aligned(idx, 4) || !aligned(cnt, 4) || !aligned(ws, 256) ||
       (key_bias && !aligned(key_bias, 4)))
     return SA_EINVAL;
@@ -299,7 +299,7 @@ SA_API sa_status sparse_attn_fused(const sa_params* p, const void* q, const void
   if (st != SA_OK) return st;
   if (g.nvk > kMaxFusedVideoBlocks) return SA_EUNSUPPORTED;
   if (!q || !k || !v || !idx || !cnt || !o || !ws) return SA_EINVAL;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 32) ||
       !aligned(idx, 4) || !aligned(cnt, 4) || !aligned(ws, 256) ||
       (key_bias && !aligned(key_bias, 4)))
     return SA_EINVAL;
@@ -376,7 +376,7 @@ SA_API sa_status sparse_attn_spark_fwd(const sa_params* p, const void* q, const 
   if (st != SA_OK) return st;
   if (uint64_t(g.H) * uint64_t(g.nblk) * kHeadDim >= (uint64_t(1) << 31)) return SA_EUNSUPPORTED;
   if (!q || !k || !v || !idx || !cnt || !o || !ws) return SA_EINVAL;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 32) ||
       !aligned(idx, 4) || !aligned(cnt, 4) || !aligned(ws, 256) ||
       (key_bias && !aligned(key_bias, 4)))
     return SA_EINVAL;

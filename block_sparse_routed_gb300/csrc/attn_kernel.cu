@@ -1021,14 +1021,17 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         tmem_ld32(tmem + lane_addr + kColO + 64u * grp + c0, o);
         tmem_wait_ld();
         if (real) {
+          // 32-byte stores (o is 32-byte aligned): whole L2 sectors, half
+          // the store instructions of 16-byte ones, each of which touches
+          // 32 rows.
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv_l, __uint_as_float(o[q4 * 8 + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv_l, __uint_as_float(o[q4 * 8 + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv_l, __uint_as_float(o[q4 * 8 + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv_l, __uint_as_float(o[q4 * 8 + 7]) * inv_l);
-            dst[c0 / 8 + q4] = w;
+          for (int q8 = 0; q8 < 2; ++q8) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(o[q8 * 16 + 2 * e]) * inv_l,
+                                 __uint_as_float(o[q8 * 16 + 2 * e + 1]) * inv_l);
+            st_global_v8(dst + c0 / 8 + 2 * q8, w);
           }
         }
       }

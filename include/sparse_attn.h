@@ -32,7 +32,9 @@
  *
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers on the current CUDA device,
- *     owned by the caller, 16-byte aligned and contiguous.  No entry point
+ *     owned by the caller, 16-byte aligned and contiguous; the output `o` of
+ *     the attention calls is 32-byte aligned (its rows are written by
+ *     32-byte stores).  No entry point
  *     allocates device memory (the one fixed scratch array of
  *     sparse_attn_plan_static is part of the loaded library).
  *   - All GPU work is enqueued on `stream`; plan and fwd never synchronise
@@ -136,8 +138,8 @@ sa_status sparse_attn_plan(const sa_params* p, const void* q, const void* k, int
  *             checked on the device before any of their blocks is loaded:
  *             1 <= cnt <= maxl, entries in [0, nblk) and strictly increasing,
  *             else SA_EINVAL (device-detected)
- *   o         BF16 [1, T, H, 128]; every row is written when the device
- *             status is SA_OK
+ *   o         BF16 [1, T, H, 128], 32-byte aligned; every row is written
+ *             when the device status is SA_OK
  *   ws        workspace of at least fwd_ws_bytes (may alias none of the
  *             tensors above)
  * Errors before launch: as sparse_attn_plan.  Device-detected conditions

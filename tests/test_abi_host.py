@@ -149,6 +149,11 @@ def test_plan_and_fwd_reject_bad_arguments_before_launch(native):
     assert lib.sparse_attn_fwd(ctypes.byref(p), A, A, A + 8, None, A, A, A, A, sz.fwd_ws_bytes, None) == E
     assert lib.sparse_attn_fwd(ctypes.byref(p), A, A, A, A + 2, A, A, A, A, sz.fwd_ws_bytes, None) == E
     assert lib.sparse_attn_fwd(ctypes.byref(p), A, A, A, None, A, A, A, A, 16, None) == E
+    # the output is written with 32-byte stores: 16-byte alignment is not enough
+    assert lib.sparse_attn_fwd(ctypes.byref(p), A, A, A, None, A, A, A + 16, A, sz.fwd_ws_bytes, None) == E
+    big = 1 << 30  # past every workspace size these calls ask for
+    assert lib.sparse_attn_spark_fwd(ctypes.byref(p), A, A, A, None, A, A, A + 16, A, big, None) == E
+    assert lib.sparse_attn_fused(ctypes.byref(p), A, A, A, None, A, A, A + 16, A, big, None) == E
     bad = _params(native, 1152, 2, 1024, 0.25, -1, "dense")
     assert lib.sparse_attn_fwd(ctypes.byref(bad), A, A, A, None, A, A, A, A, 1 << 30, None) == E
     assert lib.sparse_attn_last_device_status(None, None, ctypes.byref(ctypes.c_int())) == E
