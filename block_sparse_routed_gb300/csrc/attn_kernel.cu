@@ -882,9 +882,9 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const int kx = 4 * q4 + e;
                 const float x = (kx < nv) ? fmaf(__uint_as_float(sh[kx]), sl2, bq[e]) : -INFINITY;
                 sh[kx] = __float_as_uint(x);
-                mx = fmaxf(mx, x);
               }
             }
+            mx = fmaxf(mx, max64(sh));  // a tree, not a chain of 64 dependent maxima
             tmem_st32(scol + 64u * hh, *reinterpret_cast<uint32_t(*)[32]>(&sh[0]));
             tmem_st32(scol + 64u * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&sh[32]));
           }
