@@ -102,3 +102,14 @@ def test_fused_rejects_long_rows(bsr):
     with pytest.raises(bsr.SparseAttnError) as e:
         _native.sparse_attn_fused_ws_bytes(P.to_c())
     assert e.value.status == _native.SA_EUNSUPPORTED
+
+
+def test_fused_zero_bias_is_no_bias(bsr):
+    # an all-zero key bias takes the no-bias path: the same output bit for bit
+    # ("Add key bias to chunked Sol-Attn producers", "Contract")
+    T, H, Nv = 64 * 20 + 30, 2, 64 * 18
+    base = make_inputs(T=T, H=H, video_tokens=Nv, qk_kind="walk1d", seed=78)
+    r0, _ = both_paths(bsr, dict(base, bias=None), T, H, Nv, 0.25, 1, "dense")
+    r1, _ = both_paths(bsr, dict(base, bias=np.zeros(T, np.float32)), T, H, Nv, 0.25, 1, "dense")
+    assert r0["status"] == 0 and r1["status"] == 0
+    assert torch.equal(r0["o1"], r1["o1"]) and torch.equal(r0["o2"], r1["o2"])

@@ -160,3 +160,14 @@ def test_merged_ragged(bsr, T, Nv, mode):
     assert same.all()
     d = np.abs(gpu["o"] - o)
     assert d.max() <= parity.OUT_MAX_ABS and d.mean() <= parity.OUT_MEAN_ABS
+
+
+def test_merged_zero_bias_is_no_bias(bsr):
+    # an all-zero key bias takes the no-bias path: the same output bit for bit
+    # ("Add key bias to chunked Sol-Attn producers", "Contract")
+    T, H, Nv = 64 * 20 + 30, 2, 64 * 18
+    base = make_inputs(T=T, H=H, video_tokens=Nv, qk_kind="walk1d", seed=77)
+    none, _ = run_spark(bsr, dict(base, bias=None), T, H, Nv, 0.25, 1, "dense")
+    zero, _ = run_spark(bsr, dict(base, bias=np.zeros(T, np.float32)), T, H, Nv, 0.25, 1, "dense")
+    assert none["status"] == 0 and zero["status"] == 0
+    assert np.array_equal(none["o"], zero["o"])
