@@ -27,11 +27,12 @@
 // ring, the S buffers and every barrier phase continue across units, so the
 // next unit's loads and first MMAs overlap the current unit's tail.
 //
-// Schedule.  One thread issues tcgen05.mma at about one instruction per 105
-// cycles at this shape (M = N = 128, K = 16), slower than the tensor pipe
-// executes them (64), so two threads issue: warp 1 the S MMAs
-// (S_x = Q K_x^T) and warp 3 the PV MMAs (O += P_x V_x), each a chain on its
-// own accumulator.  Three S buffers (step x in buffer x mod 3) give the
+// Schedule.  Two threads issue the MMAs, one per dependency chain: warp 1
+// the S MMAs (S_x = Q K_x^T, which wait for K and for a free S buffer) and
+// warp 3 the PV MMAs (O += P_x V_x, which wait for P and V), each on its own
+// accumulator.  (A 16-MMA phase at this shape, M = N = 128, K = 16, takes
+// 1024 cycles from two threads and 1102 from one: the tensor pipe's rate of
+// 64 cycles per MMA, nearly.)  Three S buffers (step x in buffer x mod 3) give the
 // softmax two steps of lead: S_{x+3} is issued as soon as PV_x has completed,
 // since P_x is written as packed BF16 over the first 64 columns of S_x's
 // buffer.
