@@ -71,12 +71,63 @@ constexpr int kRouteThreads = 256;
 constexpr int kKeyChunk = 128;           // Kmean rows staged per step
 constexpr int kKcStride = kHeadDim + 1;  // padded row: conflict-free column reads
 
+// Scores of one staged key chunk (keys j0 ..): thread (qg, kg) takes query
+// blocks qg*QPT .. +QPT-1 and keys kg + NKG*e, e < KPT, of the chunk, each
+// s = sum_d Qmean[d] Kmean[d] in FP32, d = 0..127 in order, times 1/sqrt(128).
+// The query values are broadcast reads, the key values come from padded rows
+// (consecutive lanes take consecutive keys, so the reads are conflict-free).
+template <int QB, int QPT, int KPT>
+__device__ __forceinline__ void score_tile(const float* qcT, const float* kcs, float* sc, int nvk, int j0,
+                                           int tid) {
+  constexpr int NQG = QB / QPT;             // query groups
+  constexpr int NKG = kRouteThreads / NQG;  // key groups
+  const int kg = tid % NKG;
+  const int qg = tid / NKG;
+  const float inv_sqrt_d = 0.08838834764831845f;  // 1/sqrt(128)
+  // a thread whose first key is past the end has no key in this chunk
+  if (j0 + kg >= nvk) return;
+  float acc[QPT][KPT];
+#pragma unroll
+  for (int q = 0; q < QPT; ++q)
+#pragma unroll
+    for (int e = 0; e < KPT; ++e) acc[q][e] = 0.f;
+#pragma unroll 8
+  for (int d = 0; d < kHeadDim; ++d) {
+    float kv[KPT];
+#pragma unroll
+    for (int e = 0; e < KPT; ++e) kv[e] = kcs[(kg + NKG * e) * kKcStride + d];
+    // the QPT query values are contiguous and 8/16-byte aligned: vector loads
+    float qv[QPT];
+    if constexpr (QPT % 4 == 0) {
+#pragma unroll
+      for (int q = 0; q < QPT; q += 4) {
+        const float4 t = *reinterpret_cast<const float4*>(qcT + d * QB + qg * QPT + q);
+        qv[q] = t.x; qv[q + 1] = t.y; qv[q + 2] = t.z; qv[q + 3] = t.w;
+      }
+    } else {
+      static_assert(QPT == 2, "query values per thread");
+      const float2 t = *reinterpret_cast<const float2*>(qcT + d * QB + qg * QPT);
+      qv[0] = t.x; qv[1] = t.y;
+    }
+#pragma unroll
+    for (int q = 0; q < QPT; ++q)
+#pragma unroll
+      for (int e = 0; e < KPT; ++e) acc[q][e] = fmaf(qv[q], kv[e], acc[q][e]);
+  }
+#pragma unroll
+  for (int e = 0; e < KPT; ++e) {
+    const int j = j0 + kg + NKG * e;
+    if (j < nvk) {
+#pragma unroll
+      for (int q = 0; q < QPT; ++q) sc[(qg * QPT + q) * nvk + j] = acc[q][e] * inv_sqrt_d;
+    }
+  }
+}
+
 // One CTA per (QB query blocks, head).
-// Phase 1: the QB x nvk score strip in shared memory.  Each thread owns QPT
-// query blocks x KPT key blocks of every 128-key chunk and accumulates
-// s = sum_d Qmean[d] Kmean[d] in FP32, d = 0..127 in order; the query values
-// are broadcast reads, the key values come from padded rows (consecutive
-// lanes take consecutive keys, so the reads are conflict-free).
+// Phase 1: the QB x nvk score strip in shared memory, staged 128 Kmean rows
+// at a time (score_tile: QPT query blocks x KPT key blocks per thread for a
+// full chunk, one key per thread for a short last chunk).
 // Phase 2: one warp per query block turns its scores into order-preserving
 // keys (forced local blocks become key 0, below every score), finds the
 // K'-th largest key exactly by a bitwise radix search (keys held in
@@ -85,9 +136,7 @@ constexpr int kKcStride = kHeadDim + 1;  // padded row: conflict-free column rea
 // sinks.
 template <int QB, int QPT, int KPT, int KPL>
 __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
-  constexpr int NQG = QB / QPT;              // query groups
-  constexpr int NKG = kRouteThreads / NQG;   // key groups
-  static_assert(NKG * KPT == kKeyChunk, "chunk mapping");
+  static_assert((kRouteThreads / (QB / QPT)) * KPT == kKeyChunk, "chunk mapping");
   const Geometry& g = a.g;
   extern __shared__ __align__(16) float rsm[];
   float* qcT = rsm;                              // [128][QB]
@@ -125,9 +174,6 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
     }
   }
 
-  const int kg = tid % NKG;
-  const int qg = tid / NKG;
-  const float inv_sqrt_d = 0.08838834764831845f;  // 1/sqrt(128)
   for (int j0 = 0; j0 < g.nvk; j0 += kKeyChunk) {
     __syncthreads();
     // Kmean chunk: loads in batches of 8 per thread, then the stores.
@@ -151,43 +197,20 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
       }
     }
     __syncthreads();
-    // a thread whose first key is past the end has no key in this chunk
-    if (j0 + kg >= g.nvk) continue;
-    float acc[QPT][KPT];
-#pragma unroll
-    for (int q = 0; q < QPT; ++q)
-#pragma unroll
-      for (int e = 0; e < KPT; ++e) acc[q][e] = 0.f;
-#pragma unroll 8
-    for (int d = 0; d < kHeadDim; ++d) {
-      float kv[KPT];
-#pragma unroll
-      for (int e = 0; e < KPT; ++e) kv[e] = kcs[(kg + NKG * e) * kKcStride + d];
-      // the QPT query values are contiguous and 8/16-byte aligned: vector loads
-      float qv[QPT];
-      if constexpr (QPT % 4 == 0) {
-#pragma unroll
-        for (int q = 0; q < QPT; q += 4) {
-          const float4 t = *reinterpret_cast<const float4*>(qcT + d * QB + qg * QPT + q);
-          qv[q] = t.x; qv[q + 1] = t.y; qv[q + 2] = t.z; qv[q + 3] = t.w;
-        }
-      } else {
-        static_assert(QPT == 2, "query values per thread");
-        const float2 t = *reinterpret_cast<const float2*>(qcT + d * QB + qg * QPT);
-        qv[0] = t.x; qv[1] = t.y;
-      }
-#pragma unroll
-      for (int q = 0; q < QPT; ++q)
-#pragma unroll
-        for (int e = 0; e < KPT; ++e) acc[q][e] = fmaf(qv[q], kv[e], acc[q][e]);
-    }
-#pragma unroll
-    for (int e = 0; e < KPT; ++e) {
-      const int j = j0 + kg + NKG * e;
-      if (j < g.nvk) {
-#pragma unroll
-        for (int q = 0; q < QPT; ++q) sc[(qg * QPT + q) * g.nvk + j] = acc[q][e] * inv_sqrt_d;
-      }
+    const int nk = min(kKeyChunk, g.nvk - j0);
+    // A short last chunk takes one key per thread (more query blocks per
+    // thread) so that every thread has work; each score is the same ordered
+    // FP32 sum whichever tile computes it.
+    if (nk == kKeyChunk) {
+      score_tile<QB, QPT, KPT>(qcT, kcs, sc, g.nvk, j0, tid);
+    } else if (QB % 2 == 0 && nk <= kRouteThreads * 2 / QB && QPT > 2) {
+      score_tile<QB, 2, 1>(qcT, kcs, sc, g.nvk, j0, tid);
+    } else if (QB % 4 == 0 && nk <= kRouteThreads * 4 / QB && QPT > 4) {
+      score_tile<QB, (QB % 4 == 0 ? 4 : 2), 1>(qcT, kcs, sc, g.nvk, j0, tid);
+    } else if (QB % 8 == 0 && nk <= kRouteThreads * 8 / QB && (QPT > 8 || KPT > 1)) {
+      score_tile<QB, (QB % 8 == 0 ? 8 : 2), 1>(qcT, kcs, sc, g.nvk, j0, tid);
+    } else {
+      score_tile<QB, QPT, KPT>(qcT, kcs, sc, g.nvk, j0, tid);
     }
   }
   __syncthreads();
@@ -379,6 +402,8 @@ cudaError_t launch_route_topk(const PlanArgs& a, cudaStream_t s) {
   const size_t smem = route_topk_smem_bytes(a.g);
   switch (route_qb(a.g)) {
     case 32:
+      if (a.g.nvk <= 128) return launch_route_variant<32, 8, 2, 4>(a, smem, s);
+      if (a.g.nvk <= 160) return launch_route_variant<32, 8, 2, 5>(a, smem, s);
       if (a.g.nvk <= 256) return launch_route_variant<32, 8, 2, 8>(a, smem, s);
       if (a.g.nvk <= 512) return launch_route_variant<32, 8, 2, 16>(a, smem, s);
       return launch_route_variant<32, 8, 2, 32>(a, smem, s);

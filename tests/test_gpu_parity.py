@@ -253,3 +253,31 @@ def test_many_video_blocks_route(bsr):
                            sz, rows, [0])
     d = np.abs(gpu["o"][rows][:, [0]] - ref_o)
     assert d.max() <= parity.OUT_MAX_ABS
+
+
+# Video key-block counts whose last 128-key chunk is short, one per scoring
+# tile: 32 query blocks per CTA with 30, 50 and 100 keys in the last chunk;
+# 16 per CTA (nvk > 1024) with 20 and 76; 8 per CTA (nvk > 2048) with 50.
+@pytest.mark.parametrize("nvk", [30, 50, 100, 1044, 1100, 2098])
+def test_route_short_last_chunk(bsr, nvk):
+    T, H, Nv = 64 * nvk + 40, 1, 64 * nvk
+    arrays = make_inputs(T=T, H=H, video_tokens=Nv, qk_kind="walk1d", seed=nvk)
+    ratio = 0.1 if nvk < 1000 else 0.02
+    sz = O.derive_sizes(T, H, Nv, ratio, 1, "dense")
+    gpu = run_gpu(bsr, arrays, T, H, Nv, ratio, 1, "dense")
+    assert gpu["status"] == 0
+    ref = O.plan(arrays["q"], arrays["k"], sz)
+    qn = np.linalg.norm(ref["Qc"], axis=-1)[:, :, None]
+    kn = np.linalg.norm(ref["Kc"], axis=-1)[:, None, :]
+    band = 2e-5 * qn * kn / np.sqrt(128) + 1e-6
+    assert (np.abs(gpu["scores"] - ref["scores"]) <= band).all()
+    n_exact, n_tie = check_lists(gpu, ref, sz)
+    assert n_tie <= max(2, (n_exact + n_tie) // 1000)
+    if nvk <= 256:
+        # the fused route sums each score in the same order: identical lists
+        P = bsr.Params(T=T, H=H, video_tokens=Nv, topk_ratio=ratio, radius=1, tail_mode="dense")
+        q, k, v = (to_dev(arrays[n], T, H) for n in "qkv")
+        _, fidx, fcnt = bsr.sparse_attn_fused(P, q, k, v)
+        torch.cuda.synchronize()
+        assert np.array_equal(fidx.cpu().numpy().reshape(gpu["idx"].shape), gpu["idx"])
+        assert np.array_equal(fcnt.cpu().numpy().reshape(gpu["cnt"].shape), gpu["cnt"])
