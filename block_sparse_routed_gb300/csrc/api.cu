@@ -417,8 +417,10 @@ SA_API sa_status sparse_attn_spark_fwd(const sa_params* p, const void* q, const 
   r.H = g.H;
   r.P = 1;
   r.nblk = g.nblk;
+  r.lm2 = lm2;  // the log2 row for the attention kernel, written alongside lm
+  r.nvk = g.nvk;
+  r.nblkp = L.nblkp;
   if (cuda_failed(launch_spark_reweight(r, stream))) return SA_ECUDA;
-  if (cuda_failed(launch_logmass_log2(lm, lm2, g.H, g.nblk, g.nvk, L.nblkp, stream))) return SA_ECUDA;
 
   AttnArgs a;
   a.idx = idx;
@@ -473,6 +475,8 @@ SA_API sa_status sparse_attn_spark_reweight(const sa_reweight_params* p, const v
   r.H = p->H;
   r.P = p->P;
   r.nblk = static_cast<int>(nblk);
+  r.lm2 = nullptr;  // summaries only
+  r.nvk = r.nblkp = 0;
   if (cuda_failed(launch_spark_reweight(r, stream))) return SA_ECUDA;
   return SA_OK;
 }

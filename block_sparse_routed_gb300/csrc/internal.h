@@ -80,6 +80,10 @@ struct ReweightArgs {
   uint16_t* av;
   float* lm;           // [P, H, nblk]
   int T, H, P, nblk;
+  // Optional (merged forward, P = 1): lm in log2 units for the attention
+  // kernel, [H, nblkp], 0 for blocks >= nvk and the padding.
+  float* lm2;
+  int nvk, nblkp;
 };
 
 // Records a failed CUDA call for sparse_attn_last_cuda_error (thread-local,
@@ -122,8 +126,6 @@ cudaError_t launch_reblock(const ReblockArgs& r, cudaStream_t s);
 int anchor_chunks(int Nv);
 cudaError_t launch_video_query_mean(const uint16_t* q, float* partial, uint16_t* anchor, int H, int Nv,
                                     cudaStream_t s);
-cudaError_t launch_logmass_log2(const float* lm, float* lm2, int H, int nblk, int nvk, int nblkp,
-                                cudaStream_t s);
 size_t route_topk_smem_bytes(const Geometry& g);
 size_t attention_smem_bytes();
 

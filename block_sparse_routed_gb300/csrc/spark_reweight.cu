@@ -161,7 +161,17 @@ __global__ void __launch_bounds__(32 * kRwWarps, 2) spark_reweight_kernel(const 
     float kr[4];
     bf16x4(ko, kr);
     const float key = warp_sum(fmaf(a[3], kr[3], fmaf(a[2], kr[2], fmaf(a[1], kr[1], a[0] * kr[0]))));
-    if (lane == 0) r.lm[orow] = (dmax - key) * kInvSqrtD + logf(l);
+    const float lmv = (dmax - key) * kInvSqrtD + logf(l);
+    if (lane == 0) r.lm[orow] = lmv;
+    if (r.lm2 != nullptr && p == 0) {
+      // the log2 row the merged attention kernel reads, nblkp entries (the
+      // video blocks rounded up to 64): 0 past the video keys, and over any
+      // padding past the last block, which the head's last block writes
+      float* row2 = r.lm2 + static_cast<size_t>(h) * r.nblkp;
+      if (lane == 0 && b < r.nblkp) row2[b] = (b < r.nvk) ? lmv * kLog2e : 0.f;
+      if (b == r.nblk - 1)
+        for (int j = r.nblk + lane; j < r.nblkp; j += 32) row2[j] = 0.f;
+    }
   }
 }
 
@@ -225,14 +235,6 @@ __global__ void anchor_final_kernel(const float* partial, uint16_t* anchor, int 
   anchor[static_cast<size_t>(h) * kHeadDim + d] = static_cast<uint16_t>(r & 0xFFFFu);
 }
 
-// log-mass in log2 units, rows padded to `nblkp` with zeros (masked keys)
-__global__ void logmass_log2_kernel(const float* lm, float* lm2, int nblk, int nvk, int nblkp) {
-  const int h = blockIdx.y;
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= nblkp) return;
-  lm2[static_cast<size_t>(h) * nblkp + j] = (j < nvk) ? lm[static_cast<size_t>(h) * nblk + j] * kLog2e : 0.f;
-}
-
 }  // namespace
 
 int anchor_chunks(int Nv) { return (Nv + kAnchorRows - 1) / kAnchorRows; }
@@ -244,12 +246,6 @@ cudaError_t launch_video_query_mean(const uint16_t* q, float* partial, uint16_t*
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   anchor_final_kernel<<<H, kHeadDim, 0, s>>>(partial, anchor, nch, Nv);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_logmass_log2(const float* lm, float* lm2, int H, int nblk, int nvk, int nblkp,
-                                cudaStream_t s) {
-  logmass_log2_kernel<<<dim3((nblkp + 127) / 128, H), 128, 0, s>>>(lm, lm2, nblk, nvk, nblkp);
   return cudaGetLastError();
 }
 
