@@ -206,8 +206,8 @@ SA_API sa_status sparse_attn_plan(const sa_params* p, const void* q, const void*
   a.idx = idx;
   a.cnt = cnt;
   a.scores = route_scores;
+  a.status = reinterpret_cast<int32_t*>(w);  // zeroed by the pool kernel
   a.g = g;
-  if (cuda_failed(cudaMemsetAsync(ws, 0, kStatusBytes, stream))) return SA_ECUDA;
   if (cuda_failed(launch_pool(a, stream))) return SA_ECUDA;
   if (cuda_failed(launch_route_topk(a, stream))) return SA_ECUDA;
   return SA_OK;
@@ -325,6 +325,7 @@ SA_API sa_status sparse_attn_fused(const sa_params* p, const void* q, const void
   pa.idx = idx;
   pa.cnt = cnt;
   pa.scores = nullptr;
+  pa.status = nullptr;  // zeroed above (the attention kernel's counter too)
   pa.g = g;
   if (cuda_failed(launch_pool(pa, stream))) return SA_ECUDA;
   if (key_bias && cuda_failed(launch_bias_prep(key_bias, b2, status, g, stream))) return SA_ECUDA;

@@ -37,6 +37,7 @@ struct PlanArgs {
   int32_t* idx;       // [H, nq, maxl]
   int32_t* cnt;       // [H, nq]
   float* scores;      // [H, nq, nvk] or null
+  int32_t* status;    // the call's status words, zeroed by the pool kernel (or null)
   Geometry g;
 };
 

@@ -28,7 +28,20 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // 16-byte slices, so every row is read with full coalescing.  HBM-bound.
 constexpr int kPoolThreads = 256;
 
+// Programmatic dependent launch: the routing kernel is launched while the
+// pool grid runs and waits for its results (and their visibility) here.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(kPoolThreads) pool_kernel(const PlanArgs a, int nchunks) {
+  // The call's status words (the plan itself records no error) are zeroed
+  // here instead of by a separate memset.
+  if (a.status != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < kStatusBytes / 4)
+    a.status[threadIdx.x] = 0;
+  // The dependent routing grid may be launched once every pool CTA runs.
+  griddep_launch_dependents();
   const Geometry g = a.g;
   const bool isq = blockIdx.y == 0;
   const int nblocks = isq ? g.nq : g.nvk;
@@ -137,6 +150,7 @@ __device__ __forceinline__ void score_tile(const float* qcT, const float* kcs, f
 template <int QB, int QPT, int KPT, int KPL>
 __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
   static_assert((kRouteThreads / (QB / QPT)) * KPT == kKeyChunk, "chunk mapping");
+  griddep_wait();  // the block means of the pool grid
   const Geometry& g = a.g;
   extern __shared__ __align__(16) float rsm[];
   float* qcT = rsm;                              // [128][QB]
@@ -393,9 +407,19 @@ static cudaError_t launch_route_variant(const PlanArgs& a, size_t smem, cudaStre
   auto* k = route_topk_kernel<QB, QPT, KPT, KPL>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const dim3 grid((a.g.nq + QB - 1) / QB, a.g.H);
-  k<<<grid, kRouteThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  // launched as the pool grid's programmatic dependent (it starts while the
+  // pool grid finishes and waits for it in the kernel)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.g.nq + QB - 1) / QB, a.g.H);
+  cfg.blockDim = dim3(kRouteThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, a);
 }
 
 cudaError_t launch_route_topk(const PlanArgs& a, cudaStream_t s) {

@@ -132,10 +132,10 @@ SA_API sa_status sparse_attn_plan_static(const sa_params* p, const void* q, cons
   a.idx = idx;
   a.cnt = cnt;
   a.scores = route_scores;
+  // The status area starts at zero on every call (the pooling kernel clears
+  // it); the means are fully overwritten by the pooling kernel.
+  a.status = reinterpret_cast<int32_t*>(scratch);
   a.g = g;
-  // The status area must start at zero on every call; the means are fully
-  // overwritten by the pooling kernel.
-  if (cuda_failed(cudaMemsetAsync(scratch, 0, kStatusBytes, stream))) return SA_ECUDA;
   if (cuda_failed(launch_pool(a, stream))) return SA_ECUDA;
   if (cuda_failed(launch_route_topk(a, stream))) return SA_ECUDA;
   return SA_OK;
