@@ -264,6 +264,9 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   // when video block 64 chunk + u is skipped by that half's list
   auto vmask = [&](int slot) { return reinterpret_cast<unsigned long long*>(base + kOffMask) + slot * 2 * kMaxChunks; };
 
+  // launched as a programmatic dependent: the previous kernels' results
+  // (lists, status words, bias) are read only after this
+  griddep_wait();
   if (threadIdx.x == 0) {
     *s_status = *reinterpret_cast<volatile int32_t*>(a.status);
     *s_abort = 0;
@@ -1061,10 +1064,20 @@ attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+// A call's status words (error word, unit counter, nonzero-bias flag) set to
+// zero once the stream's previous kernel is done.
+__global__ void zero_status_kernel(int32_t* status) {
+  griddep_launch_dependents();
+  griddep_wait();
+  if (threadIdx.x < kStatusBytes / 4) status[threadIdx.x] = 0;
+}
+
 // Key bias: log2 conversion, the sink-only rule, and the flag (status word
 // 2) that some bias value is nonzero.
 __global__ void bias_prep_kernel(const float* __restrict__ bias, float* __restrict__ b2,
                                  int32_t* status, int T, int video_keys) {
+  griddep_launch_dependents();
+  griddep_wait();  // b2 may share memory the previous kernel reads
   const float kLog2e = 1.4426950408889634f;
   for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < T; u += gridDim.x * blockDim.x) {
     const float b = bias[u];
@@ -1094,13 +1107,17 @@ int sm_count() {
 
 size_t attention_smem_bytes() { return kSmemBytes; }
 
+cudaError_t launch_zero_status(int32_t* status, cudaStream_t s) {
+  return launch_dependent(zero_status_kernel, dim3(1), dim3(kStatusBytes / 4), 0, s, status);
+}
+
 cudaError_t launch_bias_prep(const float* bias, float* b2, int32_t* status, const Geometry& g,
                              cudaStream_t s) {
   const int threads = 256;
   int blocks = (g.T + threads - 1) / threads;
   if (blocks > 1024) blocks = 1024;
-  bias_prep_kernel<<<blocks, threads, 0, s>>>(bias, b2, status, g.T, g.nvk * kBlock);
-  return cudaGetLastError();
+  return launch_dependent(bias_prep_kernel, dim3(blocks), dim3(threads), 0, s, bias, b2, status, g.T,
+                          g.nvk * kBlock);
 }
 
 cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -1129,8 +1146,7 @@ cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const
   if (units == 0) return cudaSuccess;
   const int grid = units < sm_count() ? units : sm_count();
   if (a.merged && grid > kMaxMergedCtas) return cudaErrorInvalidConfiguration;
-  kern<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, tak, tav, a);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(grid), dim3(kThreads), kSmemBytes, s, tq, tk, tv, tak, tav, a);
 }
 
 }  // namespace sa

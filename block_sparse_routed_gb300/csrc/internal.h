@@ -87,6 +87,25 @@ struct ReweightArgs {
   int nvk, nblkp;
 };
 
+// Launches `kern` with programmatic stream serialization: it may start while
+// the stream's previous kernel finishes, and waits for that kernel on the
+// device (griddep_wait) before touching what it wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Records a failed CUDA call for sparse_attn_last_cuda_error (thread-local,
 // defined in api.cu); returns true when `e` is an error.
 bool cuda_failed(cudaError_t e);
@@ -94,6 +113,8 @@ bool cuda_failed(cudaError_t e);
 // Launchers (defined in the kernel translation units).
 cudaError_t launch_pool(const PlanArgs& a, cudaStream_t s);
 cudaError_t launch_route_topk(const PlanArgs& a, cudaStream_t s);
+// Clears a call's status words (after the stream's previous kernel).
+cudaError_t launch_zero_status(int32_t* status, cudaStream_t s);
 cudaError_t launch_bias_prep(const float* bias, float* b2, int32_t* status, const Geometry& g,
                              cudaStream_t s);
 cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -14,6 +14,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "sm103_ptx.cuh"
 
 namespace sa {
 namespace {
@@ -27,13 +28,6 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // and sums it down the block's rows; consecutive threads read consecutive
 // 16-byte slices, so every row is read with full coalescing.  HBM-bound.
 constexpr int kPoolThreads = 256;
-
-// Programmatic dependent launch: the routing kernel is launched while the
-// pool grid runs and waits for its results (and their visibility) here.
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void griddep_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
 
 __global__ void __launch_bounds__(kPoolThreads) pool_kernel(const PlanArgs a, int nchunks) {
   // The call's status words (the plan itself records no error) are zeroed
@@ -151,6 +145,7 @@ template <int QB, int QPT, int KPT, int KPL>
 __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
   static_assert((kRouteThreads / (QB / QPT)) * KPT == kKeyChunk, "chunk mapping");
   griddep_wait();  // the block means of the pool grid
+  griddep_launch_dependents();  // the forward's first kernel may start
   const Geometry& g = a.g;
   extern __shared__ __align__(16) float rsm[];
   float* qcT = rsm;                              // [128][QB]
@@ -407,19 +402,9 @@ static cudaError_t launch_route_variant(const PlanArgs& a, size_t smem, cudaStre
   auto* k = route_topk_kernel<QB, QPT, KPT, KPL>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  // launched as the pool grid's programmatic dependent (it starts while the
-  // pool grid finishes and waits for it in the kernel)
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.g.nq + QB - 1) / QB, a.g.H);
-  cfg.blockDim = dim3(kRouteThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, a);
+  // the pool grid's programmatic dependent: it starts while the pool grid
+  // finishes and waits for it in the kernel
+  return launch_dependent(k, dim3((a.g.nq + QB - 1) / QB, a.g.H), dim3(kRouteThreads), smem, s, a);
 }
 
 cudaError_t launch_route_topk(const PlanArgs& a, cudaStream_t s) {

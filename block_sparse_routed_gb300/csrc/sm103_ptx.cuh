@@ -80,6 +80,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   }
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// A grid launched with programmatic stream serialization may start while the
+// stream's previous grid still runs; griddep_wait() returns once that grid
+// has completed and its memory operations are visible.  A grid that calls
+// griddep_launch_dependents() lets its own dependent start early.  Both are
+// no-ops for a grid launched the ordinary way.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
