@@ -25,6 +25,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "sm103_ptx.cuh"
 
 namespace sa {
 namespace {
@@ -72,6 +73,8 @@ __device__ __forceinline__ void fold(float* v, int lane, int o) {
 }
 
 __global__ void __launch_bounds__(32 * kRwWarps, 2) spark_reweight_kernel(const ReweightArgs r) {
+  griddep_launch_dependents();  // the next kernel of the call may be launched
+  griddep_wait();               // (each waits for its predecessor's writes)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int64_t item = static_cast<int64_t>(blockIdx.x) * kRwWarps + warp;
   if (item >= static_cast<int64_t>(r.nblk) * r.H) return;
@@ -181,8 +184,7 @@ cudaError_t launch_spark_reweight(const ReweightArgs& r, cudaStream_t s) {
   const int64_t items = static_cast<int64_t>(r.nblk) * r.H;
   const int64_t grid = (items + kRwWarps - 1) / kRwWarps;
   if (grid == 0) return cudaSuccess;
-  spark_reweight_kernel<<<static_cast<unsigned>(grid), 32 * kRwWarps, 0, s>>>(r);
-  return cudaGetLastError();
+  return launch_dependent(spark_reweight_kernel, dim3(static_cast<unsigned>(grid)), dim3(32 * kRwWarps), 0, s, r);
 }
 
 }  // namespace sa
@@ -201,6 +203,8 @@ constexpr int kAnchorRows = 1024;  // rows per partial sum
 // dimensions 8s..8s+7 over rows r, r+16, ... of the chunk.
 __global__ void __launch_bounds__(256) anchor_partial_kernel(const uint16_t* __restrict__ q, float* partial,
                                                              int H, int Nv) {
+  griddep_launch_dependents();  // the next kernel of the call may be launched
+  griddep_wait();               // (each waits for its predecessor's writes)
   const int c = blockIdx.x, h = blockIdx.y;
   const int s = threadIdx.x % 16, r = threadIdx.x / 16;
   const int t0 = c * kAnchorRows, t1 = min(Nv, t0 + kAnchorRows);
@@ -226,6 +230,8 @@ __global__ void __launch_bounds__(256) anchor_partial_kernel(const uint16_t* __r
 }
 
 __global__ void anchor_final_kernel(const float* partial, uint16_t* anchor, int nch, int Nv) {
+  griddep_launch_dependents();  // the next kernel of the call may be launched
+  griddep_wait();               // (each waits for its predecessor's writes)
   const int h = blockIdx.x, d = threadIdx.x;
   float sum = 0.f;
   for (int c = 0; c < nch; ++c) sum += partial[(static_cast<size_t>(h) * nch + c) * kHeadDim + d];
@@ -242,11 +248,9 @@ int anchor_chunks(int Nv) { return (Nv + kAnchorRows - 1) / kAnchorRows; }
 cudaError_t launch_video_query_mean(const uint16_t* q, float* partial, uint16_t* anchor, int H, int Nv,
                                     cudaStream_t s) {
   const int nch = anchor_chunks(Nv);
-  anchor_partial_kernel<<<dim3(nch, H), 256, 0, s>>>(q, partial, H, Nv);
-  cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_dependent(anchor_partial_kernel, dim3(nch, H), dim3(256), 0, s, q, partial, H, Nv);
   if (e != cudaSuccess) return e;
-  anchor_final_kernel<<<H, kHeadDim, 0, s>>>(partial, anchor, nch, Nv);
-  return cudaGetLastError();
+  return launch_dependent(anchor_final_kernel, dim3(H), dim3(kHeadDim), 0, s, partial, anchor, nch, Nv);
 }
 
 }  // namespace sa
