@@ -29,7 +29,6 @@
 #include <vector>
 
 #include "internal.h"
-#include "sm103_ptx.cuh"
 
 namespace sa {
 namespace {
@@ -146,8 +145,6 @@ __device__ __forceinline__ void load_half4(const __half* p, float v[4]) {
 // FP16 unit rows of every token t < N of every head, [H, N, 128]: a warp per
 // eight tokens of one head, all eight rows in flight.
 __global__ void __launch_bounds__(256) reblock_unit_kernel(Samples xs, int N, int H, __half* __restrict__ xh) {
-  griddep_launch_dependents();  // the call's next kernel may be launched
-  griddep_wait();               // (each waits for its predecessor's writes)
   const int64_t w = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int groups = (N + kKeyTokens - 1) / kKeyTokens;
@@ -197,8 +194,6 @@ __global__ void __launch_bounds__(kPairThreads) reblock_pair_kernel(const __half
                                                                    int2* __restrict__ pairs, int N, int fanout,
                                                                    int L, int level,
                                                                    const __grid_constant__ LevelNodes nodes) {
-  griddep_launch_dependents();  // the call's next kernel may be launched
-  griddep_wait();               // (each waits for its predecessor's writes)
   constexpr int kWarps = kPairThreads / 32;
   // [L][132]: 16-byte rows for vector loads; 132 = 4 mod 32 words keeps the
   // eight rows a quarter-warp reads in distinct banks
@@ -270,8 +265,6 @@ __global__ void __launch_bounds__(kRbThreads) reblock_keys_kernel(const __half* 
                                                                  const int2* __restrict__ pairs,
                                                                  uint64_t* __restrict__ keys, int N, int fanout,
                                                                  int level) {
-  griddep_launch_dependents();  // the call's next kernel may be launched
-  griddep_wait();               // (each waits for its predecessor's writes)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int x = blockIdx.x * kRbWarps + warp, h = blockIdx.y;
   const int m_root = N / kBlock;
@@ -318,8 +311,6 @@ __global__ void __launch_bounds__(kT) reblock_split_kernel(const int32_t* __rest
                                                           int32_t* __restrict__ ord_out,
                                                           const uint64_t* __restrict__ keys, int N, int fanout,
                                                           int level, const __grid_constant__ LevelNodes nodes) {
-  griddep_launch_dependents();  // the call's next kernel may be launched
-  griddep_wait();               // (each waits for its predecessor's writes)
   constexpr int kNb = kReblockMaxFanout - 1;
   constexpr int kW = kT / 32;
   __shared__ uint32_t hist[kNb * 256];
@@ -485,8 +476,6 @@ __global__ void __launch_bounds__(kT) reblock_split_kernel(const int32_t* __rest
 __global__ void reblock_finish_kernel(const int32_t* __restrict__ ord0, const int32_t* __restrict__ ord1, int N,
                                       int T, int H, int fanout, int32_t* __restrict__ perm,
                                       int32_t* __restrict__ inv) {
-  griddep_launch_dependents();  // the call's next kernel may be launched
-  griddep_wait();               // (each waits for its predecessor's writes)
   const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (e >= static_cast<int64_t>(T) * H) return;
   const int h = static_cast<int>(e / T), i = static_cast<int>(e % T);
@@ -583,9 +572,8 @@ cudaError_t launch_reblock(const ReblockArgs& r, cudaStream_t stream) {
   const int depth = N > 0 ? reblock_depth(m_root, r.fanout) : 0;
   if (depth > 0) {
     const int64_t warps = static_cast<int64_t>((N + kKeyTokens - 1) / kKeyTokens) * r.H;
-    if ((e = launch_dependent(reblock_unit_kernel, dim3(static_cast<unsigned>((warps + 7) / 8)), dim3(256), 0,
-                              stream, xs, N, r.H, xh)) != cudaSuccess)
-      return e;
+    reblock_unit_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(xs, N, r.H, xh);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   for (int lv = 0; lv < depth; ++lv) {
     int max_m = 0;
@@ -593,10 +581,9 @@ cudaError_t launch_reblock(const ReblockArgs& r, cudaStream_t stream) {
     const int threads = kBlock * max_m <= 1024 ? 128 : (kBlock * max_m <= 4096 ? 512 : 1024);
     for (int pass = 0; pass < 3; ++pass) {
       if (pass == 1) {
-        if ((e = launch_dependent(reblock_keys_kernel, dim3((m_root + kRbWarps - 1) / kRbWarps, r.H),
-                                  dim3(kRbThreads), 0, stream, xh, ord[lv & 1], pairs, keys, N, r.fanout, lv)) !=
-            cudaSuccess)
-          return e;
+        reblock_keys_kernel<<<dim3((m_root + kRbWarps - 1) / kRbWarps, r.H), kRbThreads, 0, stream>>>(
+            xh, ord[lv & 1], pairs, keys, N, r.fanout, lv);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
         continue;
       }
       for (size_t k0 = 0; k0 < all.size(); k0 += kReblockMaxLevelNodes) {
@@ -605,25 +592,25 @@ cudaError_t launch_reblock(const ReblockArgs& r, cudaStream_t stream) {
         for (int k = 0; k < nodes.count; ++k) nodes.start[k] = all[k0 + k];
         const dim3 grid(nodes.count, r.H);
         if (pass == 0)
-          e = launch_dependent(reblock_pair_kernel, grid, dim3(kPairThreads),
-                               r.landmarks * kLandStride * sizeof(float), stream, xh, ord[lv & 1], pairs, N,
-                               r.fanout, r.landmarks, lv, nodes);
+          reblock_pair_kernel<<<grid, kPairThreads, r.landmarks * kLandStride * sizeof(float), stream>>>(
+              xh, ord[lv & 1], pairs, N, r.fanout, r.landmarks, lv, nodes);
         else if (threads == 128)  // CTA size follows the level's node size
-          e = launch_dependent(reblock_split_kernel<128>, grid, dim3(128), 0, stream, ord[lv & 1],
-                               ord[(lv + 1) & 1], keys, N, r.fanout, lv, nodes);
+          reblock_split_kernel<128><<<grid, 128, 0, stream>>>(ord[lv & 1], ord[(lv + 1) & 1], keys, N, r.fanout,
+                                                             lv, nodes);
         else if (threads == 512)
-          e = launch_dependent(reblock_split_kernel<512>, grid, dim3(512), 0, stream, ord[lv & 1],
-                               ord[(lv + 1) & 1], keys, N, r.fanout, lv, nodes);
+          reblock_split_kernel<512><<<grid, 512, 0, stream>>>(ord[lv & 1], ord[(lv + 1) & 1], keys, N, r.fanout,
+                                                             lv, nodes);
         else
-          e = launch_dependent(reblock_split_kernel<1024>, grid, dim3(1024), 0, stream, ord[lv & 1],
-                               ord[(lv + 1) & 1], keys, N, r.fanout, lv, nodes);
-        if (e != cudaSuccess) return e;
+          reblock_split_kernel<1024><<<grid, 1024, 0, stream>>>(ord[lv & 1], ord[(lv + 1) & 1], keys, N, r.fanout,
+                                                               lv, nodes);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
       }
     }
   }
   const int64_t total = static_cast<int64_t>(r.T) * r.H;
-  return launch_dependent(reblock_finish_kernel, dim3(static_cast<unsigned>((total + 255) / 256)), dim3(256), 0,
-                          stream, ord[0], ord[1], N, r.T, r.H, r.fanout, r.perm, r.inv);
+  reblock_finish_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(ord[0], ord[1], N, r.T, r.H,
+                                                                                       r.fanout, r.perm, r.inv);
+  return cudaGetLastError();
 }
 
 }  // namespace sa
