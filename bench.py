@@ -508,7 +508,7 @@ def run_ours(args, rank, world, local_rank):
     peak = float(peaks["bf16_tflops"])
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": profile_traffic() if name == WORKLOAD and world == 1 else None,
-                "kernel": "attention_kernel (fwd call: status clear + attention)",
+                "kernel": "attention_kernel (fwd call: status memset + attention)",
                 "peak_kind": f"{peak_kind} bf16 burst"}
 
     cpu = cpu1 = None
@@ -564,7 +564,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d_all,
                 "d2h_bytes_per_step": d2h_all, "ms_per_step": e2e_ms,
                 "pipeline": "2 buffer sets, copy-in / compute / copy-out streams"},
-        "gpu_launches": args.steps * (4 + (1 if bias is not None else 0)),  # pool, route, status clear, attention (+ bias prep)
+        "gpu_launches": args.steps * (3 + (1 if bias is not None else 0)),  # pool, route, attention (+ bias prep)
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

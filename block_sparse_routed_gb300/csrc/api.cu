@@ -236,7 +236,7 @@ SA_API sa_status sparse_attn_fwd(const sa_params* p, const void* q, const void* 
   uint8_t* w = static_cast<uint8_t*>(ws);
   int32_t* status = reinterpret_cast<int32_t*>(w);
   float* b2 = key_bias ? reinterpret_cast<float*>(w + kStatusBytes) : nullptr;
-  if (cuda_failed(launch_zero_status(static_cast<int32_t*>(ws), stream))) return SA_ECUDA;
+  if (cuda_failed(cudaMemsetAsync(ws, 0, kStatusBytes, stream))) return SA_ECUDA;
   if (key_bias && cuda_failed(launch_bias_prep(key_bias, b2, status, g, stream))) return SA_ECUDA;
 
   AttnArgs a;
@@ -314,7 +314,7 @@ SA_API sa_status sparse_attn_fused(const sa_params* p, const void* q, const void
   uint8_t* w = static_cast<uint8_t*>(ws);
   int32_t* status = reinterpret_cast<int32_t*>(w);
   float* b2 = key_bias ? reinterpret_cast<float*>(w + L.b2) : nullptr;
-  if (cuda_failed(launch_zero_status(static_cast<int32_t*>(ws), stream))) return SA_ECUDA;
+  if (cuda_failed(cudaMemsetAsync(ws, 0, kStatusBytes, stream))) return SA_ECUDA;
   // block means (the routing kernel's first half); the route runs in the
   // attention kernel's scheduler
   PlanArgs pa;
@@ -400,7 +400,7 @@ SA_API sa_status sparse_attn_spark_fwd(const sa_params* p, const void* q, const 
 
   int32_t* status = reinterpret_cast<int32_t*>(w);
   float* b2 = key_bias ? reinterpret_cast<float*>(w + L.b2) : nullptr;
-  if (cuda_failed(launch_zero_status(static_cast<int32_t*>(ws), stream))) return SA_ECUDA;
+  if (cuda_failed(cudaMemsetAsync(ws, 0, kStatusBytes, stream))) return SA_ECUDA;
   if (key_bias && cuda_failed(launch_bias_prep(key_bias, b2, status, g, stream))) return SA_ECUDA;
   // the per-head anchor, its summaries of every block, the log-mass in log2
   if (cuda_failed(launch_video_query_mean(static_cast<const uint16_t*>(q),

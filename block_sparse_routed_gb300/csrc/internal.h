@@ -113,8 +113,6 @@ bool cuda_failed(cudaError_t e);
 // Launchers (defined in the kernel translation units).
 cudaError_t launch_pool(const PlanArgs& a, cudaStream_t s);
 cudaError_t launch_route_topk(const PlanArgs& a, cudaStream_t s);
-// Clears a call's status words (after the stream's previous kernel).
-cudaError_t launch_zero_status(int32_t* status, cudaStream_t s);
 cudaError_t launch_bias_prep(const float* bias, float* b2, int32_t* status, const Geometry& g,
                              cudaStream_t s);
 cudaError_t launch_attention(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

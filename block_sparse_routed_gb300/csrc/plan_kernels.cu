@@ -145,7 +145,6 @@ template <int QB, int QPT, int KPT, int KPL>
 __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(PlanArgs a) {
   static_assert((kRouteThreads / (QB / QPT)) * KPT == kKeyChunk, "chunk mapping");
   griddep_wait();  // the block means of the pool grid
-  griddep_launch_dependents();  // the forward's first kernel may start
   const Geometry& g = a.g;
   extern __shared__ __align__(16) float rsm[];
   float* qcT = rsm;                              // [128][QB]
